@@ -1,0 +1,438 @@
+"""Pins of the oracle against facts fixed outside itself (no GPU needed).
+
+Each test names the source that fixes the expected value: a format
+specification, a library routine (torch's float8 / bf16 conversions, torch's
+scaled_dot_product_attention and logsumexp in float64), a closed form, an
+algebraic identity stated on the pages, or a hand-built fixture.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------- codecs
+def test_e4m3_decode_all_codes_match_torch(oracle_lib):
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    both_nan = np.isnan(ours) & np.isnan(ref)
+    assert np.all(both_nan | (ours == ref))
+    assert np.isnan(ours).sum() == 2  # S.1111.111 only (OCP E4M3)
+
+
+def test_e4m3_spec_values(oracle_lib):
+    # OCP 8-bit FP spec, E4M3: bias 7, max normal 448, min normal 2^-6, min subnormal 2^-9
+    d = oracle.e4m3_decode
+    assert d(0x7E) == 448.0
+    assert d(0x08) == 2.0 ** -6
+    assert d(0x01) == 2.0 ** -9
+    assert d(0x07) == 7 * 2.0 ** -9
+    assert d(0x38) == 1.0
+    assert d(0xB8) == -1.0
+    assert d(0x80) == 0.0 and math.copysign(1.0, d(0x80)) == -1.0
+    assert math.isnan(d(0x7F)) and math.isnan(d(0xFF))
+
+
+def test_e4m3_encode_matches_torch_rne(oracle_lib):
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.uniform(-448, 448, 3000), rng.standard_normal(3000) * 2.0 ** rng.integers(-12, 6, 3000),
+                        rng.uniform(-2.0 ** -7, 2.0 ** -7, 1000)]).astype(np.float32)
+    ours = oracle.e4m3_encode(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_encode_ties_to_even(oracle_lib):
+    # exact midpoints between consecutive finite codes round to the even code
+    vals = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2
+    enc = oracle.e4m3_encode(mids)
+    lo = np.arange(0x7E)
+    expect = np.where(lo % 2 == 0, lo, lo + 1)
+    assert np.array_equal(enc, expect.astype(np.uint8))
+    # and torch agrees (its fp32 -> e4m3 conversion is round-to-nearest-even)
+    ref = torch.from_numpy(mids.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(enc, ref)
+
+
+def test_e4m3_encode_saturates(oracle_lib):
+    enc = oracle.e4m3_encode(np.array([448.0, 448.5, 463.9, 470.0, 1e6, np.inf, -np.inf, -500.0]))
+    assert list(enc) == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert oracle.e4m3_encode(np.array([np.nan]))[0] == 0x7F
+
+
+def test_e4m3_roundtrip_finite_codes(oracle_lib):
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes)), codes)
+
+
+def test_bf16_decode_matches_torch(oracle_lib):
+    rng = np.random.default_rng(2)
+    bits = rng.integers(0, 1 << 16, 4000).astype(np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]  # finite
+    ours = oracle.bf16_decode(bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_ue8m0(oracle_lib):
+    # OCP MX spec E8M0: 2^(b-127), 0xFF NaN
+    d = oracle.ue8m0_decode(np.array([127, 128, 123, 0, 254], dtype=np.uint8))
+    assert list(d) == [1.0, 2.0, 1.0 / 16, 2.0 ** -127, 2.0 ** 127]
+    assert math.isnan(oracle.ue8m0_decode(np.array([255], dtype=np.uint8))[0])
+
+
+# ----------------------------------------------------------------------------- layouts
+def _read_fixture(name):
+    entries = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            entries.append(line.split())
+    return entries
+
+
+def test_fp8_page_layout_golden(oracle_lib):
+    ent = _read_fixture("fp8_448_page_ps2.txt")
+    pb = int([e for e in ent if e[0] == "page_bytes"][0][1])
+    info = oracle.layout_info(oracle.LAYOUT_FP8_448, 2)
+    assert info["page_bytes"] == pb and info["dqk"] == 512 and info["row_bytes"] == 576
+    page = np.zeros((1, pb), dtype=np.uint8)
+    for e in ent:
+        if e[0] == "row1_nope":
+            page[0, 576 + int(e[1])] = int(e[2], 0)
+        elif e[0] == "row1_scale":
+            page[0, 2 * 576 + 8 + int(e[1])] = int(e[2], 0)
+        elif e[0] == "row1_rope":
+            v = int(e[2], 0)
+            o = 576 + 448 + 2 * int(e[1])
+            page[0, o], page[0, o + 1] = v & 0xFF, v >> 8
+    k = oracle.decode_row(page, oracle.LAYOUT_FP8_448, 2, 0, 1)
+    expect = np.zeros(512)
+    for e in ent:
+        if e[0] == "expect":
+            expect[int(e[1])] = float(e[2])
+    assert np.array_equal(k, expect)
+    # row 0 decodes to zeros (its scale bytes are 0 -> 2^-127, codes 0)
+    assert np.array_equal(oracle.decode_row(page, oracle.LAYOUT_FP8_448, 2, 0, 0), np.zeros(512))
+
+
+def test_page_sizes(oracle_lib):
+    # page_bytes a multiple of the row size ("MLA" API page of HALOps, kv_cache parameter)
+    assert oracle.layout_info(0, 64)["page_bytes"] == 64 * 1152
+    assert oracle.layout_info(1, 64)["page_bytes"] == 37440 and 37440 % 576 == 0
+    assert oracle.layout_info(2, 64)["page_bytes"] == 41600 and 41600 % 640 == 0
+    for ps in (1, 2, 16, 64, 128, 256):
+        for lay, rb in ((1, 576), (2, 640)):
+            pb = oracle.layout_info(lay, ps)["page_bytes"]
+            assert pb % rb == 0 and pb >= ps * (rb + 8) and pb - ps * (rb + 8) < rb
+            assert workloads.page_bytes(lay, ps) == pb
+
+
+# ----------------------------------------------------------------------------- attention algebra
+def test_mha_equals_mqa_absorbed(oracle_lib):
+    """Absorbed MQA form == naive MHA form ("mla_attention.py", module docstring:
+    Compute Friendly Approach vs Data-Movement Friendly Approach), fp64, tiny
+    random weights. ql_nope = einsum(q_nope, W_UK); o = einsum(sdpa_o, W_UV)."""
+    rng = np.random.default_rng(3)
+    N, P, R, Lkv, V, S = 4, 16, 8, 32, 12, 9
+    W_UK = rng.standard_normal((Lkv, N, P))
+    W_UV = rng.standard_normal((Lkv, N, V))
+    q_nope = rng.standard_normal((N, P))
+    q_pe = rng.standard_normal((N, R))
+    kv_c = rng.standard_normal((S, Lkv))
+    k_pe = rng.standard_normal((S, R))
+    scale = 1.0 / math.sqrt(P + R)
+    rows = np.concatenate([kv_c, k_pe], axis=1)
+    for n in range(N):
+        ql = np.einsum("h,lh->l", q_nope[n], W_UK[:, n, :])
+        o_lat, lse_mqa = oracle.attend(np.concatenate([ql, q_pe[n]]), rows, Lkv, scale)
+        o_mqa = o_lat @ W_UV[:, n, :]
+        # MHA with per-head keys/values, computed with torch's float64 SDPA
+        k_nope = kv_c @ W_UK[:, n, :]
+        v = kv_c @ W_UV[:, n, :]
+        qh = torch.tensor(np.concatenate([q_nope[n], q_pe[n]]))[None, None, None, :]
+        kh = torch.tensor(np.concatenate([k_nope, k_pe], axis=1))[None, None]
+        vh = torch.tensor(v)[None, None]
+        o_mha = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, scale=scale)[0, 0, 0].numpy()
+        s = (kh[0, 0] @ qh[0, 0, 0]) * scale
+        lse_mha = torch.logsumexp(s, 0).item()
+        assert np.allclose(o_mqa, o_mha, rtol=0, atol=1e-10)
+        assert abs(lse_mqa - lse_mha) < 1e-10
+
+
+def test_single_key(oracle_lib):
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal(576)
+    k = rng.standard_normal((1, 576))
+    out, lse = oracle.attend(q, k, 512, 0.1)
+    assert np.array_equal(out, k[0, :512])
+    assert abs(lse - 0.1 * float(q @ k[0])) < 1e-12
+
+
+def test_identical_keys(oracle_lib):
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal(576)
+    k = rng.standard_normal(576)
+    L = 37
+    out, lse = oracle.attend(q, np.tile(k, (L, 1)), 512, 0.07)
+    assert np.allclose(out, k[:512], atol=1e-13)
+    assert abs(lse - (0.07 * float(q @ k) + math.log(L))) < 1e-12
+
+
+def test_empty_candidate_set(oracle_lib):
+    out, lse = oracle.attend(np.ones(576), np.zeros((0, 576)), 512, 0.1, sink=1.0)
+    assert np.all(out == 0) and lse == -math.inf
+
+
+def test_split_merge_equals_unsplit(oracle_lib):
+    """merge_attn_states semantics ("mla_attention.py", Chunked Prefill; an empty
+    partial is a zero output with -inf lse, neutralize_empty_context_partials)."""
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal(576)
+    rows = rng.standard_normal((200, 576))
+    full, lse_full = oracle.attend(q, rows, 512, 0.05)
+    for cuts in ([0, 1, 200], [0, 64, 128, 200], [0, 17, 17, 99, 200], [0, 200, 200]):
+        parts, lses = [], []
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            o, l = oracle.attend(q, rows[a:b], 512, 0.05)
+            parts.append(o)
+            lses.append(l)
+        out, lse = oracle.combine(np.array(parts), np.array(lses))
+        assert np.allclose(out, full, atol=1e-12)
+        assert abs(lse - lse_full) < 1e-12
+    out, lse = oracle.combine(np.zeros((3, 512)), np.full(3, -np.inf))
+    assert np.all(out == 0) and lse == -math.inf
+
+
+def test_sink_enters_denominator_only(oracle_lib):
+    """attn_sink: per-head logit added to the softmax denominator ("MLA" API page
+    of HALOps, mla_attention)."""
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(576)
+    rows = rng.standard_normal((50, 576))
+    base, lse0 = oracle.attend(q, rows, 512, 0.05)
+    for sink in (-3.0, 0.0, 2.5):
+        o, lse = oracle.attend(q, rows, 512, 0.05, sink=sink)
+        z = math.exp(lse0)
+        assert np.allclose(o, base * z / (z + math.exp(sink)), atol=1e-13)
+        assert lse == lse0
+        # combine applies the same factor after merging sink-free partials
+        o1, l1 = oracle.attend(q, rows[:20], 512, 0.05)
+        o2, l2 = oracle.attend(q, rows[20:], 512, 0.05)
+        oc, lc = oracle.combine(np.array([o1, o2]), np.array([l1, l2]), sink=sink)
+        assert np.allclose(oc, o, atol=1e-12) and abs(lc - lse) < 1e-12
+    o, lse = oracle.attend(q, rows, 512, 0.05, sink=-math.inf)
+    assert np.array_equal(o, base)
+
+
+# ----------------------------------------------------------------------------- paged decode
+def _torch_reference(w, causal=False):
+    """Brute force with torch float64 SDPA over rows gathered by plain indexing."""
+    cfg = w.cfg
+    ps = cfg.page_size
+    kv16 = torch.from_numpy(w.kv_cache.view(np.int16).copy()).view(torch.bfloat16).double()
+    kv16 = kv16.reshape(w.kv_cache.shape[0], ps, 576)
+    q = torch.from_numpy(w.q.view(np.int16).copy()).view(torch.bfloat16).double()
+    T, N, D = q.shape
+    out = torch.zeros(T, N, 512, dtype=torch.float64)
+    lse = torch.zeros(T, N, dtype=torch.float64)
+    for t in range(T):
+        b, i = t // cfg.sq, t % cfg.sq
+        L = int(w.seqlens[b])
+        lim = L - cfg.sq + i + 1 if causal else L
+        pos = torch.arange(lim)
+        pages = torch.from_numpy(w.block_table[b]).long()[pos // ps]
+        K = kv16[pages, pos % ps]
+        s = (q[t] @ K.T) * cfg.sm_scale
+        lse[t] = torch.logsumexp(s, dim=1)
+        out[t] = torch.nn.functional.scaled_dot_product_attention(q[t][:, None], K[None].expand(N, -1, -1),
+                                                                  K[None, :, :512].expand(N, -1, -1),
+                                                                  scale=cfg.sm_scale)[:, 0]
+    return out.numpy(), lse.numpy()
+
+
+def test_tiny_decode_matches_torch_sdpa(oracle_lib):
+    w = workloads.generate(workloads.tiny())
+    out, lse = oracle.mla_decode(w.q, w.kv_cache, 0, 16, w.block_table, w.seqlens, 1, w.cfg.sm_scale)
+    ro, rl = _torch_reference(w)
+    assert np.allclose(out, ro, atol=1e-12)
+    assert np.allclose(lse, rl, atol=1e-12)
+
+
+def test_verify_causal_matches_torch_sdpa(oracle_lib):
+    cfg = workloads.verify(batch=3, heads=16, seqlens=(4, 70, 131), page_size=16)
+    w = workloads.generate(cfg)
+    out, lse = oracle.mla_decode(w.q, w.kv_cache, 0, 16, w.block_table, w.seqlens, 4, cfg.sm_scale, causal=True)
+    ro, rl = _torch_reference(w, causal=True)
+    assert np.allclose(out, ro, atol=1e-12)
+    assert np.allclose(lse, rl, atol=1e-12)
+
+
+def test_causal_reductions(oracle_lib):
+    """Causal verify (bottom-right, seq_len = context_len + query_len,
+    "mla_attention.py", MLACommonMetadata): s_q = 1 equals dense; token i equals
+    a dense decode over the first L - s_q + i + 1 rows."""
+    cfg = workloads.verify(batch=2, heads=16, seqlens=(40, 97), page_size=16)
+    w = workloads.generate(cfg)
+    sq = 4
+    out, lse = oracle.mla_decode(w.q, w.kv_cache, 0, 16, w.block_table, w.seqlens, sq, cfg.sm_scale, causal=True)
+    for b in range(2):
+        for i in range(sq):
+            t = b * sq + i
+            Li = int(w.seqlens[b]) - sq + i + 1
+            o1, l1 = oracle.mla_decode(w.q[t:t + 1], w.kv_cache, 0, 16, w.block_table[b:b + 1],
+                                       np.array([Li], np.int32), 1, cfg.sm_scale)
+            assert np.allclose(out[t], o1[0], atol=1e-13) and np.allclose(lse[t], l1[0], atol=1e-13)
+    # s_q = 1 causal == dense
+    o2, l2 = oracle.mla_decode(w.q[::sq], w.kv_cache, 0, 16, w.block_table, w.seqlens, 1, cfg.sm_scale, causal=True)
+    o3, l3 = oracle.mla_decode(w.q[::sq], w.kv_cache, 0, 16, w.block_table, w.seqlens, 1, cfg.sm_scale)
+    assert np.array_equal(o2, o3) and np.array_equal(l2, l3)
+
+
+def test_sparse_reductions(oracle_lib):
+    """Sparse indices (request-local positions, "Implementation:Sgl project
+    Sglang Flash MLA", I/O Contract): the identity list equals dense; order does
+    not matter; -1 and out-of-range entries are skipped; a duplicate counts twice."""
+    cfg = workloads.dsv4(batch=2, seqlens=(90, 150), len_dist="fixed", page_size=16)
+    w = workloads.generate(cfg)
+    L0, L1 = 90, 150
+    dense, dl = oracle.mla_decode(w.q, w.kv_cache, 1, 16, w.block_table, w.seqlens, 1, cfg.sm_scale, sink=w.sink)
+    topk = 160
+    idx = np.full((2, topk), -1, np.int32)
+    idx[0, :L0] = np.arange(L0)
+    idx[1, :L1] = np.arange(L1)
+    sp, sl = oracle.mla_decode(w.q, w.kv_cache, 1, 16, w.block_table, w.seqlens, 1, cfg.sm_scale, sink=w.sink,
+                               indices=idx)
+    assert np.allclose(sp, dense, atol=1e-13) and np.allclose(sl, dl, atol=1e-13)
+    rng = np.random.default_rng(8)
+    idx2 = idx.copy()
+    idx2[0] = rng.permutation(idx2[0])
+    idx2[1] = rng.permutation(idx2[1])
+    sp2, sl2 = oracle.mla_decode(w.q, w.kv_cache, 1, 16, w.block_table, w.seqlens, 1, cfg.sm_scale, sink=w.sink,
+                                 indices=idx2)
+    assert np.allclose(sp2, dense, atol=1e-12) and np.allclose(sl2, dl, atol=1e-12)
+    idx3 = idx.copy()
+    idx3[0, L0:L0 + 5] = [L0, L0 + 7, 10000, -5, -1]   # all invalid for request 0
+    sp3, _ = oracle.mla_decode(w.q, w.kv_cache, 1, 16, w.block_table, w.seqlens, 1, cfg.sm_scale, sink=w.sink,
+                               indices=idx3)
+    assert np.array_equal(sp3, sp)
+    # duplicate: index 3 listed twice == a row list with row 3 repeated
+    idx4 = np.full((1, 4), -1, np.int32)
+    idx4[0, :3] = [3, 3, 9]
+    o4, l4 = oracle.mla_decode(w.q[:1], w.kv_cache, 1, 16, w.block_table[:1], w.seqlens[:1], 1, cfg.sm_scale,
+                               indices=idx4)
+    rows = np.stack([oracle.decode_row(w.kv_cache, 1, 16, w.block_table[0, j // 16], j % 16) for j in (3, 3, 9)])
+    qd = oracle.bf16_decode(w.q[0, 5])
+    oa, la = oracle.attend(qd, rows, 512, cfg.sm_scale)
+    assert np.allclose(o4[0, 5], oa, atol=1e-13) and abs(l4[0, 5] - la) < 1e-13
+
+
+def test_selected_rows_match_full(oracle_lib):
+    w = workloads.generate(workloads.tiny())
+    full, fl = oracle.mla_decode(w.q, w.kv_cache, 0, 16, w.block_table, w.seqlens, 1, w.cfg.sm_scale)
+    sel = (np.array([1, 0, 1], np.int32), np.array([3, 15, 0], np.int32))
+    o, l = oracle.mla_decode(w.q, w.kv_cache, 0, 16, w.block_table, w.seqlens, 1, w.cfg.sm_scale, select=sel)
+    for k in range(3):
+        assert np.array_equal(o[k], full[sel[0][k], sel[1][k]]) and l[k] == fl[sel[0][k], sel[1][k]]
+
+
+def test_empty_request(oracle_lib):
+    w = workloads.generate(workloads.dsv4(batch=2, seqlens=(0, 70), len_dist="fixed", page_size=16))
+    o, l = oracle.mla_decode(w.q, w.kv_cache, 1, 16, w.block_table, w.seqlens, 1, w.cfg.sm_scale, sink=w.sink)
+    assert np.all(o[0] == 0) and np.all(l[0] == -np.inf)
+    assert np.all(np.isfinite(l[1]))
+
+
+# ----------------------------------------------------------------------------- kv write
+def test_group_exponent_is_minimal(oracle_lib):
+    for a in [1e-10, 1e-3, 0.5, 1.0, 447.9, 448.0, 448.1, 896.0, 1e5, 3.0e38]:
+        e = oracle.group_exponent(a)
+        assert 448.0 * 2.0 ** e >= a and 448.0 * 2.0 ** (e - 1) < a
+
+
+def test_kv_write_fp8_matches_torch_quantization(oracle_lib):
+    """fp8 row quantization: one ue8m0 (power-of-two) scale per 64 NoPE elements
+    ("MLA" API page of HALOps, supported config); codes must equal torch's
+    float8_e4m3fn rounding of x * 2^-e."""
+    rng = np.random.default_rng(9)
+    for layout, nope in ((1, 448), (2, 512)):
+        ps = 16
+        info = oracle.layout_info(layout, ps)
+        kv = np.zeros((3, info["page_bytes"]), np.uint8)
+        n = 20
+        x = (rng.standard_normal((n, info["dqk"])) * 2.0 ** rng.integers(-20, 20, (n, 1))).astype(np.float32)
+        x[3, :64] = 0.0            # all-zero group -> eps
+        x[4, 64:128] *= 1e-30      # tiny group
+        bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        xb = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+        slots = rng.permutation(3 * ps)[:n].astype(np.int32)
+        slots[5] = -1              # skipped
+        out = oracle.kv_write(bits, slots, kv, layout, ps)
+        for r in range(n):
+            if slots[r] < 0:
+                continue
+            p, o = divmod(int(slots[r]), ps)
+            row = out[p, o * info["row_bytes"]:(o + 1) * info["row_bytes"]]
+            sc = out[p, ps * info["row_bytes"] + o * 8: ps * info["row_bytes"] + o * 8 + 8]
+            for g in range(nope // 64):
+                grp = xb[r, g * 64:(g + 1) * 64]
+                amax = max(np.abs(grp).max(), float(np.float32(1e-10)))
+                e = int(sc[g]) - 127
+                assert 448.0 * 2.0 ** e >= amax > 448.0 * 2.0 ** (e - 1)
+                ref = torch.from_numpy((grp * 2.0 ** -e).astype(np.float32)).to(torch.float8_e4m3fn)
+                assert np.array_equal(row[g * 64:(g + 1) * 64], ref.view(torch.uint8).numpy())
+            assert np.all(sc[nope // 64:] == 0)
+            assert np.array_equal(row[nope:].view(np.uint16), bits[r, nope:])
+        # the skipped slot's bytes are untouched
+        touched = {int(s) for s in slots if s >= 0}
+        for s in range(3 * ps):
+            if s not in touched:
+                p, o = divmod(s, ps)
+                assert np.all(out[p, o * info["row_bytes"]:(o + 1) * info["row_bytes"]] == 0)
+
+
+def test_kv_write_bf16_is_bit_copy(oracle_lib):
+    rng = np.random.default_rng(10)
+    bits = rng.integers(0, 1 << 16, (5, 576)).astype(np.uint16)
+    kv = np.zeros((2, 16 * 1152), np.uint8)
+    slots = np.array([0, 17, 31, 5, 16], np.int32)
+    out = oracle.kv_write(bits, slots, kv, 0, 16)
+    for r, s in enumerate(slots):
+        p, o = divmod(int(s), 16)
+        assert np.array_equal(out[p, o * 1152:(o + 1) * 1152].view(np.uint16), bits[r])
+
+
+def test_kv_write_then_decode_roundtrip_error(oracle_lib):
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((8, 512)).astype(np.float32)
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xb = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    kv = oracle.kv_write(bits, np.arange(8, dtype=np.int32), np.zeros((1, oracle.layout_info(1, 8)["page_bytes"]),
+                                                                      np.uint8), 1, 8)
+    for r in range(8):
+        k = oracle.decode_row(kv, 1, 8, 0, r)
+        for g in range(7):
+            grp = xb[r, g * 64:(g + 1) * 64]
+            e = oracle.group_exponent(max(np.abs(grp).max(), 1e-10))
+            # E4M3 relative half-ulp is 2^-4 for normals; absolute floor 2^-10 (half subnormal step) * 2^e
+            err = np.abs(k[g * 64:(g + 1) * 64] - grp)
+            assert np.all(err <= np.maximum(np.abs(grp) * 2.0 ** -4, 2.0 ** (e - 10)) + 1e-300)
+        assert np.array_equal(k[448:], xb[r, 448:])
+
+
+def test_kv_gather_matches_decode_row(oracle_lib):
+    w = workloads.generate(workloads.dsv4(batch=2, seqlens=(33, 70), len_dist="fixed", page_size=16))
+    g = oracle.kv_gather(w.kv_cache, 1, 16, w.block_table[1], 70)
+    for j in (0, 15, 16, 69):
+        assert np.array_equal(g[j], oracle.decode_row(w.kv_cache, 1, 16, w.block_table[1, j // 16], j % 16))
