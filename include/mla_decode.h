@@ -1,0 +1,210 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) paged-latent MLA decode library.
+ *
+ * The library computes Multi-head Latent Attention decode in its absorbed
+ * ("data-movement friendly", MQA) form: each of N query heads carries
+ * q = [ql_nope (512) | q_pe (64)] and attends over one shared latent row
+ * [kv_c (512) | k_pe (64)] per context token, with V = kv_c
+ * ("mla_attention.py · tduncan/Nvidia-Optimization-Stack-VLLM", module
+ * docstring, section "Data-Movement Friendly Approach"). The interface follows
+ * the FlashMLA statement of the problem — a host planner that turns
+ * cache_seqlens into tile-scheduler metadata and split counts, then a decode
+ * call over (q, paged k_cache, block_table, cache_seqlens, softmax_scale,
+ * causal, indices) returning (out, softmax_lse)
+ * ("Implementation:Sgl project Sglang Flash MLA", Signature and I/O Contract) —
+ * and the HALOps conventions of caller-owned buffers, in-place outputs and one
+ * workspace ("MLA" API page of HALOps, mla_attention / mla_workspace).
+ *
+ * Conventions (all entry points):
+ *  - Return 0 on success or a negative MLA_ERR_* code; no exception crosses the
+ *    ABI. mla_last_error() returns a thread-local message for the last failure.
+ *  - "device" pointers are CUDA device (or managed) memory owned by the caller;
+ *    "host" pointers are ordinary host memory. Nothing is freed or kept.
+ *  - Device work is enqueued on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream) and is asynchronous. mla_decode,
+ *    mla_combine, mla_kv_write and mla_kv_gather perform no host
+ *    synchronisation and no device allocation.
+ *  - bf16 = IEEE bfloat16 bit patterns (uint16); all row-major, contiguous.
+ *
+ * KV layouts (one page = page_size rows, page_size a power of two >= 8):
+ *  MLA_KV_BF16_576      row = [kv_c 512 | k_pe 64] bf16 (1152 B);
+ *                       page_bytes = page_size * 1152. K = row[0:576], V = row[0:512].
+ *  MLA_KV_FP8_448_UE8M0 row = [448 e4m3 NoPE | 64 bf16 RoPE] (576 B); after the
+ *                       rows, page_size 8-byte scale slots (7 ue8m0 bytes, one per
+ *                       64 NoPE elements, + 1 zero byte); page_bytes = page_size*584
+ *                       rounded up to a multiple of 576 ("MLA" API page of HALOps,
+ *                       mla_attention, kv_cache parameter). K = V = the 512-wide row.
+ *  MLA_KV_FP8_512_UE8M0 the same with 512 e4m3 NoPE (640 B rows, 8 scale bytes);
+ *                       page_bytes = page_size*648 rounded up to a multiple of 640.
+ *                       K = [dequantised 512 | RoPE 64], V = K[0:512].
+ *  A NoPE value is e4m3(byte) * 2^(scale_byte - 127).
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARG (-1)          /* null pointer, bad size, misalignment */
+#define MLA_ERR_UNSUPPORTED (-2)          /* valid but outside what the kernels handle */
+#define MLA_ERR_WORKSPACE_TOO_SMALL (-3)
+#define MLA_ERR_CUDA (-4)                 /* a CUDA runtime/driver call failed */
+#define MLA_ERR_DEVICE_CHECK (-5)         /* a kernel reported a bad input or a timed-out wait */
+#define MLA_ERR_CAPACITY (-6)             /* a caller-provided host array is too short */
+
+/* Bits of the device status word (mla_read_status). */
+#define MLA_STATUS_WAIT_TIMEOUT 1u        /* a pipeline wait gave up after ~2 s */
+#define MLA_STATUS_BAD_PAGE 2u            /* a block_table entry needed for a row < L is outside [0, num_pages) */
+
+typedef enum {
+  MLA_KV_BF16_576 = 0,
+  MLA_KV_FP8_448_UE8M0 = 1,
+  MLA_KV_FP8_512_UE8M0 = 2
+} mla_kv_layout;
+
+/* Sizes the kernels are built for. */
+#define MLA_DV 512              /* value / output width per head */
+#define MLA_BLOCK_ROWS 64       /* KV rows per tile (planner block) */
+#define MLA_GROUP_ROWS 64       /* query rows (token x head) per CTA work item */
+#define MLA_WORKSPACE_HEADER 256
+
+typedef struct {
+  int32_t num_partitions;   /* rows of sched produced */
+  int32_t groups;           /* query-row groups per request = ceil(q_tokens*heads / 64) */
+  int32_t total_splits;     /* num_splits[batch]: sum over requests of their split counts */
+  int32_t max_splits;       /* largest split count of one request */
+  size_t workspace_bytes;   /* device workspace mla_decode needs for this plan */
+} mla_plan_info;
+
+/* Page size in bytes of a layout (see above). Host only. */
+int mla_page_bytes(mla_kv_layout layout, int32_t page_size, int64_t* page_bytes);
+
+/*
+ * Split-KV planner (host). The pages fix its inputs and outputs
+ * (get_mla_metadata: cache_seqlens, query tokens x heads, topk ->
+ * tile_scheduler_metadata, num_splits; "Implementation:Sgl project Sglang
+ * Flash MLA", Signature); the rule is this library's own:
+ *  - G = ceil(q_tokens_per_req*num_heads / 64) query-row groups per request;
+ *    P = max(1, num_sms / G) partitions share the SMs.
+ *  - request b has nb_b = max(1, ceil(K_b / 64)) KV blocks, K_b = topk if
+ *    topk > 0 else cache_seqlens[b]; its cost is nb_b + 2.
+ *  - payload = max(ceil(sum cost / P), 3); with min_splits > 1 it is capped at
+ *    max(1, min_b nb_b / min_splits) + 2 (integer division), which cuts every
+ *    request of >= min_splits blocks into >= min_splits splits.
+ *  - partitions are filled greedily in request order; a partition that cannot
+ *    take the rest of a request takes (budget - 2) blocks of it and closes.
+ * Outputs (host arrays):
+ *  sched [num_partitions][8] int32: begin_req, begin_blk, end_req, end_blk
+ *        (exclusive, request-major order), first_split (split index of the first
+ *        segment within begin_req), 0, 0, 0.
+ *  num_splits [batch + 1] int32: prefix sums of per-request split counts.
+ * Pass sched == NULL to only fill *info. Returns MLA_ERR_CAPACITY (with *info
+ * filled) if sched_capacity < info->num_partitions.
+ * cache_seqlens: host [batch]; batch >= 1; q_tokens_per_req >= 1; num_heads
+ * >= 1; topk >= 0; min_splits >= 1; num_sms >= 1 (the SM count of the device
+ * mla_decode will run on).
+ */
+int mla_decode_plan(const int32_t* cache_seqlens, int32_t batch, int32_t q_tokens_per_req, int32_t num_heads,
+                    int32_t topk, int32_t min_splits, int32_t num_sms, int32_t* sched, int32_t sched_capacity,
+                    int32_t* num_splits, mla_plan_info* info);
+
+/*
+ * Decode (device). out[t, n, :] and lse[t, n] for every query token t of every
+ * request and head n: softmax over the request's candidate KV rows of
+ * sm_scale * <q[t, n, :], K_j>, applied to V_j
+ * ("mla_attention.py · tduncan/Nvidia-Optimization-Stack-VLLM", module docstring,
+ * "Data-Movement Friendly Approach"; "Implementation:Sgl project Sglang Flash
+ * MLA", I/O Contract).
+ *  q            device bf16 [T = batch*q_tokens_per_req, num_heads, Dqk]
+ *               (Dqk = 576, or 512 for MLA_KV_FP8_448_UE8M0), 16-byte aligned.
+ *  kv_cache     device uint8 [num_pages, page_bytes(layout, page_size)], 16-B aligned.
+ *  block_table  device int32 [batch, max_pages]: page of each page-sized block.
+ *  cache_seqlens device int32 [batch]: L_b, context rows including the query
+ *               tokens' own new rows (seq_len = context_len + query_len,
+ *               "mla_attention.py", MLACommonMetadata).
+ *  sm_scale     softmax scale of the scores.
+ *  sink         device float [num_heads] per-head sink logit added to the
+ *               softmax denominator only, or NULL ("MLA" API page of HALOps,
+ *               mla_attention, attn_sink). lse does not include it.
+ *  indices      device int32 [T, topk] request-local KV positions, or NULL for
+ *               dense decode; entries outside [0, L_b) are skipped, duplicates
+ *               count twice; causal is ignored with indices. With indices and
+ *               q_tokens_per_req > 1, num_heads must be a multiple of 64.
+ *  causal       nonzero: query token i of a request sees rows j <= L_b - s_q + i
+ *               (draft tokens at consecutive positions, "MLA" API page of
+ *               HALOps, mla_attention, draft_tokens).
+ *  sched, num_splits, num_partitions, total_splits: from mla_decode_plan with
+ *               the same cache_seqlens/topk/heads/tokens, copied to the device.
+ *  workspace    device, >= info.workspace_bytes, 256-B aligned; its first 256
+ *               bytes hold the status word and must be zeroed once
+ *               (mla_workspace_init) before first use.
+ *  out          device bf16 [T, num_heads, 512]; lse device float [T, num_heads]
+ *               (natural log; -inf and out = 0 for an empty candidate set).
+ * num_heads must be 16, 32, 48 or a multiple of 64; q_tokens_per_req*num_heads
+ * <= 4096. Requests split by the plan are merged by mla_combine on the same
+ * stream inside this call.
+ */
+int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
+               const int32_t* block_table, int32_t max_pages, const int32_t* cache_seqlens, int32_t batch,
+               int32_t q_tokens_per_req, int32_t num_heads, float sm_scale, const float* sink,
+               const int32_t* indices, int32_t topk, int32_t causal, const int32_t* sched,
+               const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
+               size_t workspace_bytes, void* out, float* lse, void* stream);
+
+/*
+ * Split combine (device): for every request whose split count
+ * (num_splits[b+1] - num_splits[b]) is at least 2, merge its partials by
+ * log-sum-exp — lse = ln sum_s e^(lse_s), out = sum_s e^(lse_s - lse) o_s, a
+ * partial with lse_s = -inf carrying no weight ("mla_attention.py", Chunked
+ * Prefill: merge_attn_states; neutralize_empty_context_partials) — then apply
+ * the sink once: out *= 1 / (1 + e^(sink - lse)). Requests with one split are
+ * left untouched.
+ *  part_out device float [total_splits, rows_per_req, 512]; part_lse device
+ *  float [total_splits, rows_per_req]; split s of request b is row block
+ *  num_splits[b] + s. rows_per_req = q_tokens_per_req * num_heads; the head of
+ *  row r is r % num_heads.
+ */
+int mla_combine(const float* part_out, const float* part_lse, const int32_t* num_splits, int32_t batch,
+                int32_t rows_per_req, int32_t num_heads, const float* sink, void* out, float* lse, void* stream);
+
+/*
+ * KV-row write (device): scatter n new rows into their pages ("MLA" API page of
+ * HALOps, mla_attention: "RMSNorm + RoPE + KV cache write"; kv_cache parameter).
+ *  rows   device bf16 [n, row_elems], already RMSNorm'd (and RoPE'd);
+ *         row_elems = 576 (layouts 0 and 2) or 512 (layout 1: 448 NoPE | 64 RoPE).
+ *  slots  device int32 [n]: page * page_size + offset; negative slots are skipped.
+ * Layout 0 copies the bits. fp8 layouts: per 64-element NoPE group,
+ * amax = max(max|x|, 1e-10f), e = the smallest integer with 448 * 2^e >= amax,
+ * scale byte = e + 127, code = e4m3 round-to-nearest-even, saturating, of
+ * x * 2^-e; the RoPE part is copied as bf16.
+ */
+int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cache, mla_kv_layout layout,
+                 int64_t num_pages, int32_t page_size, void* stream);
+
+/*
+ * Page gather (device, a test export): out[j, :] = decoded K row j of one
+ * request (block_table_row device int32 [max_pages]) for j < length, as float
+ * [length, Dqk]. Rows whose page is out of range are written as NaN.
+ */
+int mla_kv_gather(const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
+                  const int32_t* block_table_row, int32_t max_pages, int32_t length, float* out, void* stream);
+
+/* Zero the workspace status header (enqueued on stream). */
+int mla_workspace_init(void* workspace, void* stream);
+
+/* Synchronise `stream`, read the status word into *status (MLA_STATUS_* bits);
+ * clear it if reset != 0. Returns MLA_ERR_DEVICE_CHECK when a bit is set. */
+int mla_read_status(void* workspace, uint32_t* status, int32_t reset, void* stream);
+
+/* Thread-local message describing the last nonzero return of this thread. */
+const char* mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_DECODE_H_ */

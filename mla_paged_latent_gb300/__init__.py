@@ -1,0 +1,200 @@
+"""Python binding of the GB300 paged-latent MLA decode library.
+
+Thin argument marshalling over the C ABI in include/mla_decode.h: every step of
+the decode path runs in the library's CUDA kernels. PyTorch supplies device
+memory and streams only. The functions keep the C names.
+
+If the compiled library is missing, every entry point raises: there is no CPU
+fallback. Build it with ``python -m mla_paged_latent_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import numpy as np
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+MLA_KV_BF16_576 = 0
+MLA_KV_FP8_448_UE8M0 = 1
+MLA_KV_FP8_512_UE8M0 = 2
+DQK = {0: 576, 1: 512, 2: 576}
+ROW_ELEMS = {0: 576, 1: 512, 2: 576}
+DV = 512
+WORKSPACE_HEADER = 256
+
+MLA_OK = 0
+ERRORS = {-1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "WORKSPACE_TOO_SMALL", -4: "CUDA", -5: "DEVICE_CHECK",
+          -6: "CAPACITY"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("num_partitions", ctypes.c_int32), ("groups", ctypes.c_int32), ("total_splits", ctypes.c_int32),
+                ("max_splits", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
+
+
+EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_combine", "mla_kv_write", "mla_kv_gather",
+           "mla_workspace_init", "mla_read_status", "mla_last_error"]
+
+
+def load(path: str | None = None):
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build the CUDA library first (python -m mla_paged_latent_gb300.build)")
+        lib = ctypes.CDLL(p)
+        V, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.mla_page_bytes.argtypes = [I32, I32, ctypes.POINTER(I64)]
+        lib.mla_decode_plan.argtypes = [V, I32, I32, I32, I32, I32, I32, V, I32, V, ctypes.POINTER(_PlanInfo)]
+        lib.mla_decode.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32, V, V, I32, I32,
+                                   V, SZ, V, V, V]
+        lib.mla_combine.argtypes = [V, V, V, I32, I32, I32, V, V, V, V]
+        lib.mla_kv_write.argtypes = [V, V, I32, V, I32, I64, I32, V]
+        lib.mla_kv_gather.argtypes = [V, I32, I64, I32, V, I32, I32, V, V]
+        lib.mla_workspace_init.argtypes = [V, V]
+        lib.mla_read_status.argtypes = [V, ctypes.POINTER(ctypes.c_uint32), I32, V]
+        lib.mla_last_error.restype = ctypes.c_char_p
+        for name in EXPORTS[:-1]:
+            getattr(lib, name).restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != MLA_OK:
+        raise MlaError(rc, load().mla_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _require_cuda(*tensors):
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors passed to the device entry points must live on the GPU")
+
+
+def mla_page_bytes(layout: int, page_size: int) -> int:
+    out = ctypes.c_int64()
+    _check(load().mla_page_bytes(layout, page_size, ctypes.byref(out)))
+    return out.value
+
+
+@dataclasses.dataclass
+class Plan:
+    sched: np.ndarray            # int32 [num_partitions, 8]
+    num_splits: np.ndarray       # int32 [batch + 1]
+    num_partitions: int
+    groups: int
+    total_splits: int
+    max_splits: int
+    workspace_bytes: int
+
+
+def mla_decode_plan(cache_seqlens, q_tokens_per_req: int, num_heads: int, topk: int = 0, min_splits: int = 1,
+                    num_sms: int | None = None) -> Plan:
+    """Host planner. cache_seqlens: host int array [batch]."""
+    lib = load()
+    sl = np.ascontiguousarray(np.asarray(cache_seqlens).astype(np.int32).ravel())
+    if num_sms is None:
+        import torch
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    info = _PlanInfo()
+    _check(lib.mla_decode_plan(sl.ctypes.data_as(ctypes.c_void_p), sl.shape[0], q_tokens_per_req, num_heads, topk,
+                               min_splits, num_sms, None, 0, None, ctypes.byref(info)))
+    sched = np.zeros((info.num_partitions, 8), dtype=np.int32)
+    ns = np.zeros(sl.shape[0] + 1, dtype=np.int32)
+    _check(lib.mla_decode_plan(sl.ctypes.data_as(ctypes.c_void_p), sl.shape[0], q_tokens_per_req, num_heads, topk,
+                               min_splits, num_sms, sched.ctypes.data_as(ctypes.c_void_p), info.num_partitions,
+                               ns.ctypes.data_as(ctypes.c_void_p), ctypes.byref(info)))
+    return Plan(sched, ns, info.num_partitions, info.groups, info.total_splits, info.max_splits, info.workspace_bytes)
+
+
+def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens, q_tokens_per_req: int,
+               sm_scale: float, sched, num_splits, num_partitions: int, total_splits: int, workspace, out, lse,
+               sink=None, indices=None, causal: bool = False, stream=None):
+    """Enqueue decode (+ split combine) on `stream`. All tensors on the GPU:
+    q bf16 [T, N, Dqk]; kv_cache uint8 [num_pages, page_bytes]; block_table int32 [B, max_pages];
+    cache_seqlens int32 [B]; sched int32 [P, 8]; num_splits int32 [B+1]; workspace uint8;
+    out bf16 [T, N, 512]; lse float32 [T, N]; sink float32 [N] or None; indices int32 [T, topk] or None."""
+    _require_cuda(q, kv_cache, block_table, cache_seqlens, sched, num_splits, workspace, out, lse, sink, indices)
+    T, N, D = q.shape
+    B = cache_seqlens.shape[0]
+    topk = 0 if indices is None else int(indices.shape[-1])
+    _check(load().mla_decode(_ptr(q), _ptr(kv_cache), layout, kv_cache.shape[0], page_size, _ptr(block_table),
+                             block_table.shape[1], _ptr(cache_seqlens), B, q_tokens_per_req, N, float(sm_scale),
+                             _ptr(sink), _ptr(indices), topk, int(bool(causal)), _ptr(sched), _ptr(num_splits),
+                             num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
+                             _stream(stream)))
+
+
+def mla_combine(part_out, part_lse, num_splits, rows_per_req: int, num_heads: int, out, lse, sink=None,
+                stream=None):
+    _require_cuda(part_out, part_lse, num_splits, out, lse, sink)
+    B = num_splits.shape[0] - 1
+    _check(load().mla_combine(_ptr(part_out), _ptr(part_lse), _ptr(num_splits), B, rows_per_req, num_heads,
+                              _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def mla_kv_write(rows, slots, kv_cache, layout: int, page_size: int, stream=None):
+    _require_cuda(rows, slots, kv_cache)
+    _check(load().mla_kv_write(_ptr(rows), _ptr(slots), slots.shape[0], _ptr(kv_cache), layout, kv_cache.shape[0],
+                               page_size, _stream(stream)))
+
+
+def mla_kv_gather(kv_cache, layout: int, page_size: int, block_table_row, length: int, out, stream=None):
+    _require_cuda(kv_cache, block_table_row, out)
+    _check(load().mla_kv_gather(_ptr(kv_cache), layout, kv_cache.shape[0], page_size, _ptr(block_table_row),
+                                block_table_row.shape[0], length, _ptr(out), _stream(stream)))
+
+
+def mla_workspace_init(workspace, stream=None):
+    _require_cuda(workspace)
+    _check(load().mla_workspace_init(_ptr(workspace), _stream(stream)))
+
+
+def mla_read_status(workspace, reset: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device status word (raises if nonzero)."""
+    _require_cuda(workspace)
+    st = ctypes.c_uint32()
+    _check(load().mla_read_status(_ptr(workspace), ctypes.byref(st), int(reset), _stream(stream)))
+    return st.value
+
+
+def alloc_workspace(nbytes: int, device="cuda"):
+    """A 256-byte aligned uint8 workspace with its status header zeroed."""
+    import torch
+    ws = torch.empty(max(int(nbytes), WORKSPACE_HEADER), dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    mla_workspace_init(ws)
+    return ws

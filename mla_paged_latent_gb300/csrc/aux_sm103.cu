@@ -1,0 +1,215 @@
+// Split combine, KV-row write and page gather kernels for sm_103a.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mla_kernels.h"
+#include "ptx_sm103.cuh"
+
+namespace mla {
+namespace {
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+  return static_cast<uint16_t>(f32x2_to_bf16x2(x, 0.f) & 0xFFFFu);
+}
+__device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// ----------------------------------------------------------------------------- combine
+// One warp per query row of a request that the plan split into >= 2 pieces:
+// lse = ln sum_s e^(lse_s); out = sum_s e^(lse_s - lse) o_s ("mla_attention.py ·
+// tduncan/Nvidia-Optimization-Stack-VLLM", Chunked Prefill: merge_attn_states;
+// an empty partial has lse = -inf and weight 0); then the sink factor
+// 1 / (1 + e^(sink - lse)) ("MLA" API page of HALOps, mla_output_proj: the
+// split-KV LSE combine receives attn_sink).
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
+                                                      const float* __restrict__ part_lse,
+                                                      const int32_t* __restrict__ num_splits, int R, int heads,
+                                                      const float* __restrict__ sink, uint16_t* __restrict__ out,
+                                                      float* __restrict__ lse) {
+  const int b = blockIdx.y;
+  const int s0 = num_splits[b];
+  const int ns = num_splits[b + 1] - s0;
+  if (ns < 2) return;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= R) return;
+  const int lane = threadIdx.x & 31;
+  float mx = -INFINITY;
+  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, part_lse[(int64_t)(s0 + s) * R + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const int64_t orow = (int64_t)b * R + row;
+  if (mx == -INFINITY) {
+    for (int d = lane; d < 512; d += 32) out[orow * 512 + d] = 0;
+    if (lane == 0) lse[orow] = -INFINITY;
+    return;
+  }
+  float tot = 0.f;
+  for (int s = lane; s < ns; s += 32) tot += expf(part_lse[(int64_t)(s0 + s) * R + row] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const float lse_tot = mx + logf(tot);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float ls = part_lse[(int64_t)(s0 + s) * R + row];
+    if (ls == -INFINITY) continue;
+    const float w = expf(ls - lse_tot);
+    const float4* src = reinterpret_cast<const float4*>(part_out + ((int64_t)(s0 + s) * R + row) * 512);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = src[k * 32 + lane];
+      acc[4 * k + 0] += w * v.x;
+      acc[4 * k + 1] += w * v.y;
+      acc[4 * k + 2] += w * v.z;
+      acc[4 * k + 3] += w * v.w;
+    }
+  }
+  float f = 1.f;
+  if (sink != nullptr) f = 1.f / (1.f + expf(sink[row % heads] - lse_tot));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t lo = f32x2_to_bf16x2(acc[4 * k] * f, acc[4 * k + 1] * f);
+    const uint32_t hi = f32x2_to_bf16x2(acc[4 * k + 2] * f, acc[4 * k + 3] * f);
+    *reinterpret_cast<uint2*>(out + orow * 512 + (k * 32 + lane) * 4) = make_uint2(lo, hi);
+  }
+  if (lane == 0) lse[orow] = lse_tot;
+}
+
+// ----------------------------------------------------------------------------- kv write
+// 448 * 2^e as fp32 (exact; +inf once it exceeds the fp32 range).
+__device__ __forceinline__ float pow2x448(int e) {
+  const int E = e + 8 + 127;  // 448 = 1.75 * 2^8
+  if (E >= 255) return __uint_as_float(0x7F800000u);
+  if (E <= 0) return 0.f;
+  return __uint_as_float((static_cast<uint32_t>(E) << 23) | 0x600000u);
+}
+// Smallest e with 448 * 2^e >= a (a >= 1e-10), clamped to [-127, 127]; decided by
+// exact comparisons of powers of two.
+__device__ __forceinline__ int group_exponent(float a) {
+  if (!(a <= 3.4028235e38f)) return 127;
+  int e = static_cast<int>((__float_as_uint(a) >> 23) & 0xFFu) - 127 - 8;
+  while (e < 127 && !(pow2x448(e) >= a)) ++e;
+  while (e > -127 && pow2x448(e - 1) >= a) --e;
+  return e;
+}
+// 2^-e as fp32 (exact for e in [-127, 126]).
+__device__ __forceinline__ float pow2neg(int e) {
+  const int E = 127 - e;
+  if (E >= 255) return __uint_as_float(0x7F800000u);
+  if (E <= 0) return __uint_as_float(0x00400000u >> (-E));
+  return __uint_as_float(static_cast<uint32_t>(E) << 23);
+}
+
+// One warp per new row ("MLA" API page of HALOps, mla_attention: KV cache write
+// of the RMSNorm'd row; kv_cache parameter for the layout).
+__global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restrict__ rows,
+                                                       const int32_t* __restrict__ slots, int n,
+                                                       uint8_t* __restrict__ kv, int layout, int64_t num_pages,
+                                                       int page_size, int64_t page_bytes) {
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= n) return;
+  const int64_t slot = slots[r];
+  if (slot < 0) return;
+  const int64_t page = slot / page_size;
+  if (page >= num_pages) return;
+  const int off = static_cast<int>(slot % page_size);
+  if (layout == 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(rows + (int64_t)r * 576);
+    uint4* dst = reinterpret_cast<uint4*>(kv + page * page_bytes + (int64_t)off * 1152);
+    for (int c = lane; c < 72; c += 32) dst[c] = src[c];
+    return;
+  }
+  const int nope = layout == 1 ? 448 : 512;
+  const int row_elems = layout == 1 ? 512 : 576;
+  const int row_bytes = layout == 1 ? 576 : 640;
+  const uint16_t* x = rows + (int64_t)r * row_elems;
+  uint8_t* dst = kv + page * page_bytes + (int64_t)off * row_bytes;
+  uint32_t sbytes[2] = {0u, 0u};
+  for (int g = 0; g < nope / 64; ++g) {
+    const uint32_t two = *reinterpret_cast<const uint32_t*>(x + g * 64 + 2 * lane);
+    const float x0 = bf16_to_f32(two & 0xFFFFu), x1 = bf16_to_f32(two >> 16);
+    float a = fmaxf(fabsf(x0), fabsf(x1));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    a = fmaxf(a, 1e-10f);
+    const int e = group_exponent(a);
+    const float sc = pow2neg(e);
+    uint16_t codes;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(codes) : "f"(x1 * sc), "f"(x0 * sc));
+    *reinterpret_cast<uint16_t*>(dst + g * 64 + 2 * lane) = codes;
+    sbytes[g >> 2] |= static_cast<uint32_t>(e + 127) << (8 * (g & 3));
+  }
+  // RoPE part: 64 bf16 copied
+  if (lane < 8)
+    reinterpret_cast<uint4*>(dst + nope)[lane] = reinterpret_cast<const uint4*>(x + nope)[lane];
+  if (lane == 0) {
+    uint2* sp = reinterpret_cast<uint2*>(kv + page * page_bytes + (int64_t)page_size * row_bytes + off * 8);
+    *sp = make_uint2(sbytes[0], sbytes[1]);
+  }
+}
+
+// ----------------------------------------------------------------------------- gather
+__global__ void __launch_bounds__(128) kv_gather_kernel(const uint8_t* __restrict__ kv, int layout,
+                                                        int64_t num_pages, int page_size, int64_t page_bytes,
+                                                        const int32_t* __restrict__ bt_row, int max_pages,
+                                                        int length, float* __restrict__ out) {
+  const int j = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= length) return;
+  const int dqk = layout == 1 ? 512 : 576;
+  float* o = out + (int64_t)j * dqk;
+  const int pi = j / page_size;
+  const int64_t page = pi < max_pages ? bt_row[pi] : -1;
+  if (page < 0 || page >= num_pages) {
+    for (int d = lane; d < dqk; d += 32) o[d] = __uint_as_float(0x7FC00000u);
+    return;
+  }
+  const int off = j % page_size;
+  if (layout == 0) {
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(kv + page * page_bytes + (int64_t)off * 1152);
+    for (int d = lane; d < 576; d += 32) o[d] = bf16_to_f32(src[d]);
+    return;
+  }
+  const int nope = layout == 1 ? 448 : 512;
+  const int row_bytes = layout == 1 ? 576 : 640;
+  const uint8_t* src = kv + page * page_bytes + (int64_t)off * row_bytes;
+  const uint8_t* sc = kv + page * page_bytes + (int64_t)page_size * row_bytes + off * 8;
+  for (int d = 2 * lane; d < nope; d += 64) {
+    const uint32_t two = *reinterpret_cast<const uint16_t*>(src + d);
+    const float2 v = e4m3x2_to_f32x2(two);
+    const float s = ue8m0_to_f32(sc[d >> 6]);
+    o[d] = v.x * s;
+    o[d + 1] = v.y * s;
+  }
+  const uint16_t* rope = reinterpret_cast<const uint16_t*>(src + nope);
+  for (int d = lane; d < 64; d += 32) o[nope + d] = bf16_to_f32(rope[d]);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
+                           int rows_per_req, int heads, const float* sink, uint16_t* out, float* lse,
+                           cudaStream_t stream) {
+  if (batch <= 0 || rows_per_req <= 0) return cudaSuccess;
+  dim3 grid((rows_per_req + 7) / 8, batch);
+  combine_kernel<<<grid, 256, 0, stream>>>(part_out, part_lse, num_splits, rows_per_req, heads, sink, out, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout,
+                            int64_t num_pages, int page_size, int64_t page_bytes, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  kv_write_kernel<<<(n + 3) / 4, 128, 0, stream>>>(rows, slots, n, kv, layout, num_pages, page_size, page_bytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
+                             const int32_t* bt_row, int max_pages, int length, float* out, cudaStream_t stream) {
+  if (length <= 0) return cudaSuccess;
+  kv_gather_kernel<<<(length + 3) / 4, 128, 0, stream>>>(kv, layout, num_pages, page_size, page_bytes, bt_row,
+                                                         max_pages, length, out);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,601 @@
+// Paged-latent MLA decode kernel for sm_103a (GB300).
+//
+// Computes, for every query row (token t, head n) of a request, the softmax of
+// sm_scale * <q, K_j> over the request's candidate KV rows and its weighted sum
+// of V_j = K_j[0:512] — the absorbed ("data-movement friendly", MQA) form of
+// MLA ("mla_attention.py · tduncan/Nvidia-Optimization-Stack-VLLM", module
+// docstring, "Data-Movement Friendly Approach") over a paged cache addressed
+// through block_table ("Implementation:Sgl project Sglang Flash MLA", I/O
+// Contract), with an optional per-head sink in the denominator ("MLA" API page
+// of HALOps, mla_attention, attn_sink), causal draft tokens and top-k indices.
+//
+// One persistent CTA per SM processes work items (partition p, query group g):
+// 64 query rows of one request against the KV blocks of the partition's
+// segments. Per 64-row KV tile:
+//   S   = Q K^T      tcgen05 MMA, M = 128 (query rows; rows >= 64 unused),
+//                    N = 64 KV rows, K = 576 / 512, fp32 accumulator in TMEM
+//   P   = online softmax of S (exp2 domain, lazy rescale when the running max
+//                    grows by more than 2^8), written as bf16 to shared memory
+//   O^T += V^T P^T   tcgen05 MMA, M = 128 value dims (4 blocks), N = query rows,
+//                    K = 64 KV rows, fp32 accumulator in TMEM (256 columns)
+// The transposed output accumulator keeps O for 64 query rows x 512 dims in
+// half of TMEM, leaving room for two S buffers so that S(j+1) overlaps the
+// softmax of tile j.
+//
+// Warp roles (512 threads):
+//   warp 0      TMA producer: Q once per unit, KV tiles through block_table (bf16 dense)
+//   warp 1      MMA issuer (one thread)
+//   warp 2      TMEM allocator
+//   warps 4-7   softmax (warps 4,5: one query row per thread) + O rescale + epilogue
+//   warps 8-15  converters: fp8 -> bf16 dequantisation and sparse row gathers
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mla_kernels.h"
+#include "ptx_sm103.cuh"
+
+namespace mla {
+namespace {
+
+constexpr uint32_t kSlab = 8192;  // 64 rows x 128 B (64 bf16), SW128
+constexpr int kNumBars = 16;
+enum Bar {
+  kQFull = 0,
+  kQEmpty = 1,
+  kKvFull = 2,    // +stage
+  kKvEmpty = 4,   // +stage
+  kSFull = 6,     // +buffer
+  kSFree = 8,     // +buffer
+  kPFull = 10,    // +stage
+  kPvDone = 12,
+  kOFull = 13,
+  kOFree = 14,
+  kFinal = 15
+};
+
+struct Misc {
+  uint64_t bar[kNumBars];
+  uint32_t tmem_base;
+  int abort;
+  int pad0, pad1;
+  float alpha[2][64];  // per-stage so tile j+1 cannot overwrite what tile j's rescale still reads
+  float inv[64];
+  float lse2[64];
+  uint8_t mask[2][8];  // sparse / gathered row validity per stage, one byte per 8 rows
+};
+
+template <int LAYOUT, bool TMA_KV>
+struct Cfg {
+  static constexpr int kNslab = (LAYOUT == 1) ? 8 : 9;
+  static constexpr int kNope = (LAYOUT == 1) ? 448 : 512;
+  static constexpr uint32_t kQBytes = kNslab * kSlab;
+  static constexpr uint32_t kStageBytes = kNslab * kSlab;
+  static constexpr uint32_t kOffStage = kQBytes;
+  // P^T (64 query rows x 64 KV rows bf16) lives in the RoPE slab of its stage when
+  // the row has 9 slabs (V only needs slabs 0-7); otherwise in two extra slabs.
+  static constexpr bool kPInStage = (kNslab == 9);
+  static constexpr uint32_t kOffP = kQBytes + 2 * kStageBytes;
+  static constexpr uint32_t kOffMisc = kOffP + (kPInStage ? 0 : 2 * kSlab);
+  static constexpr uint32_t kSmem = kOffMisc + sizeof(Misc) + 1024;
+  static constexpr int kChunks = (LAYOUT == 0) ? 72 : (kNope / 16 + 8);  // 16-B chunks per stored row
+  static constexpr int kChunksPerThread = kChunks / 4;
+  __device__ static uint32_t stage(uint32_t base, int st) { return base + kOffStage + st * kStageBytes; }
+  __device__ static uint32_t parea(uint32_t base, int st) {
+    return kPInStage ? stage(base, st) + 8 * kSlab : base + kOffP + st * kSlab;
+  }
+};
+
+__device__ __forceinline__ int num_blocks(const DecodeParams& P, int r) {
+  const int K = P.topk > 0 ? P.topk : P.seqlens[r];
+  const int nb = (K + kBlockRows - 1) / kBlockRows;
+  return nb < 1 ? 1 : nb;
+}
+
+// Segments (request, block range, split index) of one partition, in order.
+template <typename F>
+__device__ __forceinline__ void for_each_unit(const DecodeParams& P, int part, F&& f) {
+  const int* s = P.sched + 8 * part;
+  const int b0 = s[0], k0 = s[1], b1 = s[2], k1 = s[3], fs = s[4];
+  for (int r = b0; r < P.batch && (r < b1 || (r == b1 && k1 > 0)); ++r) {
+    const int nb = num_blocks(P, r);
+    const int lo = (r == b0) ? k0 : 0;
+    const int hi = (r == b1) ? (k1 < nb ? k1 : nb) : nb;
+    if (hi <= lo) continue;
+    f(r, lo, hi, (r == b0) ? fs : 0);
+  }
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int LAYOUT, bool TMA_KV>
+__global__ void __launch_bounds__(kDecodeThreads, 1)
+    mla_decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap q_map,
+                      const __grid_constant__ CUtensorMap kv_map) {
+  using C = Cfg<LAYOUT, TMA_KV>;
+  constexpr int NS = C::kNslab;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_addr(smem);
+  Misc* misc = reinterpret_cast<Misc*>(smem + C::kOffMisc);
+  auto bar = [&](int i) -> uint32_t { return smem_addr(&misc->bar[i]); };
+  volatile int* abort_flag = &misc->abort;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const bool sparse = P.indices != nullptr;
+
+  if (tid == 0) {
+    mbar_init(bar(kQFull), 1);
+    mbar_init(bar(kQEmpty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kKvFull + s), TMA_KV ? 1 : 256);
+      mbar_init(bar(kKvEmpty + s), 1);
+      mbar_init(bar(kSFull + s), 1);
+      mbar_init(bar(kSFree + s), 64);
+      mbar_init(bar(kPFull + s), 128);
+    }
+    mbar_init(bar(kPvDone), 1);
+    mbar_init(bar(kOFull), 1);
+    mbar_init(bar(kOFree), 128);
+    mbar_init(bar(kFinal), 1);
+    misc->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_addr(&misc->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc->tmem_base;
+  const uint32_t tmem_o = tmem;          // O^T: 4 blocks x 64 columns
+  const uint32_t tmem_s = tmem + 256;    // S: 2 buffers x 64 columns
+
+  const int G = P.groups;
+  const int R = P.rows_per_req;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&q_map);
+      if (TMA_KV) tma_prefetch_desc(&kv_map);
+      int it = 0, u = 0;
+      const int box_rows = P.page_size < kBlockRows ? P.page_size : kBlockRows;
+      const int nbox = kBlockRows / box_rows;
+      const uint32_t qbytes = NS * P.qbox_rows * 128;
+      for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
+        const int part = w / G, g = w % G;
+        for_each_unit(P, part, [&](int r, int lo, int hi, int) {
+          if (*abort_flag) return;
+          if (u > 0 && !mbar_wait(bar(kQEmpty), (u - 1) & 1, abort_flag, P.status)) return;
+          mbar_arrive_expect_tx(bar(kQFull), qbytes);
+          const int row0 = r * R + g * kGroupRows;
+          for (int s = 0; s < NS; ++s) tma_load_2d(sb + s * kSlab, &q_map, s * 64, row0, bar(kQFull));
+          ++u;
+          if (!TMA_KV) {
+            it += hi - lo;
+            return;
+          }
+          const int L = P.seqlens[r];
+          for (int j = lo; j < hi; ++j, ++it) {
+            const int st = it & 1;
+            if (it >= 2 && !mbar_wait(bar(kKvEmpty + st), ((it >> 1) - 1) & 1, abort_flag, P.status)) return;
+            int pages[8];  // page_size >= 8, so at most 64 / 8 boxes
+            uint32_t bytes = 0;
+            for (int k = 0; k < nbox; ++k) {
+              const int pos0 = j * kBlockRows + k * box_rows;
+              int page = -1;
+              if (pos0 < L) {
+                const int pi = pos0 >> P.log2_ps;
+                page = pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1;
+                if (page < 0 || page >= P.num_pages) {
+                  atomicOr(P.status, 2u);
+                  page = -1;
+                }
+              }
+              pages[k] = page;
+              if (page >= 0) bytes += NS * box_rows * 128;
+            }
+            mbar_arrive_expect_tx(bar(kKvFull + st), bytes);
+            const uint32_t dst = C::stage(sb, st);
+            for (int k = 0; k < nbox; ++k) {
+              if (pages[k] < 0) continue;
+              const int in_page = (j * kBlockRows + k * box_rows) & (P.page_size - 1);
+              for (int s = 0; s < NS; ++s)
+                tma_load_3d(dst + s * kSlab + k * box_rows * 128, &kv_map, s * 64, in_page, pages[k],
+                            bar(kKvFull + st));
+            }
+          }
+        });
+      }
+      // drain: wait for copies that may still be in flight after an abort
+      if (*abort_flag) {
+        if (u > 0) mbar_wait_drain(bar(kQFull), (u - 1) & 1);
+        for (int k = 1; k <= 2 && it - k >= 0; ++k) mbar_wait_drain(bar(kKvFull + ((it - k) & 1)), ((it - k) >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
+      int it = 0, u = 0;
+      for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
+        const int part = w / G, g = w % G;
+        int rows_g = R - g * kGroupRows;
+        rows_g = rows_g > kGroupRows ? kGroupRows : rows_g;
+        const int nq = (rows_g + 15) & ~15;
+        const uint32_t idesc_o = idesc_bf16_f32(128, nq, 1, 0);
+        for_each_unit(P, part, [&](int r, int lo, int hi, int) {
+          if (*abort_flag) return;
+          const int ntile = hi - lo;
+          auto issue_pv = [&](int itp, bool first) -> bool {
+            const int st = itp & 1;
+            if (!mbar_wait(bar(kPFull + st), (itp >> 1) & 1, abort_flag, P.status)) return false;
+            if (first && u > 0 && !mbar_wait(bar(kOFree), (u - 1) & 1, abort_flag, P.status)) return false;
+            tc_fence_after();
+            const uint32_t vs = C::stage(sb, st);
+            const uint32_t pa = C::parea(sb, st);
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = sdesc_sw128(vs + 2 * blk * kSlab + kk * 2048, kSlab, 1024);
+                const uint64_t b = sdesc_sw128(pa + kk * 32, 16, 1024);
+                mma_bf16_ss(tmem_o + blk * 64, a, b, idesc_o, (first && kk == 0) ? 0u : 1u);
+              }
+            }
+            mma_commit(bar(kKvEmpty + st));
+            mma_commit(bar(kPvDone));
+            return true;
+          };
+          if (!mbar_wait(bar(kQFull), u & 1, abort_flag, P.status)) return;
+          for (int jj = 0; jj < ntile; ++jj) {
+            const int itj = it + jj;
+            const int st = itj & 1;
+            if (!mbar_wait(bar(kKvFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+            if (itj >= 2 && !mbar_wait(bar(kSFree + st), ((itj >> 1) - 1) & 1, abort_flag, P.status)) return;
+            tc_fence_after();
+            const uint32_t ks = C::stage(sb, st);
+            const uint32_t d = tmem_s + st * 64;
+#pragma unroll 1
+            for (int s = 0; s < NS; ++s) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = sdesc_sw128(sb + s * kSlab + kk * 32, 16, 1024);
+                const uint64_t b = sdesc_sw128(ks + s * kSlab + kk * 32, 16, 1024);
+                mma_bf16_ss(d, a, b, idesc_s, (s | kk) ? 1u : 0u);
+              }
+            }
+            mma_commit(bar(kSFull + st));
+            if (jj == ntile - 1) mma_commit(bar(kQEmpty));
+            if (jj >= 1 && !issue_pv(itj - 1, jj == 1)) return;
+          }
+          if (!issue_pv(it + ntile - 1, ntile == 1)) return;
+          mma_commit(bar(kOFull));
+          it += ntile;
+          ++u;
+        });
+      }
+      // make sure every MMA issued by this thread has finished before TMEM is freed
+      mma_commit(bar(kFinal));
+      mbar_wait_drain(bar(kFinal), 0);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int wt = tid - 128;                 // 0..127, TMEM lane of this thread
+    const uint32_t lane_off = static_cast<uint32_t>((wt & ~31)) << 16;
+    const bool row_thread = wt < 64;
+    const int row = wt;
+    int it = 0, u = 0;
+    for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
+      const int part = w / G, g = w % G;
+      int rows_g = R - g * kGroupRows;
+      rows_g = rows_g > kGroupRows ? kGroupRows : rows_g;
+      const int nq = (rows_g + 15) & ~15;
+      for_each_unit(P, part, [&](int r, int lo, int hi, int sidx) {
+        if (*abort_flag) return;
+        const int L = P.seqlens[r];
+        const int grow = g * kGroupRows + row;          // query row within the request
+        const bool valid_row = row_thread && row < rows_g;
+        const int tok = grow / P.heads;
+        int lim = L;
+        if (P.causal && !sparse) {
+          lim = L - P.sq + tok + 1;
+          lim = lim > L ? L : lim;
+        }
+        float m_run = -INFINITY, l_run = 0.f;
+        const int ntile = hi - lo;
+        for (int jj = 0; jj < ntile; ++jj) {
+          const int itj = it + jj;
+          const int st = itj & 1;
+          const int j = lo + jj;
+          const bool first = jj == 0;
+          bool need = false;
+          if (row_thread) {
+            if (!mbar_wait(bar(kSFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+            if (!mbar_wait(bar(kKvFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+            tc_fence_after();
+            uint32_t sr[64];
+            {
+              uint32_t t16[16];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                tmem_ld16(tmem_s + st * 64 + lane_off + c * 16, t16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sr[c * 16 + i] = t16[i];
+              }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(kSFree + st));
+            float s[64];
+            uint64_t vmask = 0;
+            if (sparse || !TMA_KV) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) vmask |= static_cast<uint64_t>(misc->mask[st][k]) << (8 * k);
+            }
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              bool ok;
+              if (sparse) ok = (vmask >> c) & 1ull;
+              else ok = (j * kBlockRows + c) < lim;
+              ok = ok && valid_row;
+              s[c] = ok ? __uint_as_float(sr[c]) * P.scale_log2 : -INFINITY;
+              mt = fmaxf(mt, s[c]);
+            }
+            const float m_new = (mt > m_run + 8.0f) ? mt : m_run;
+            need = (m_new != m_run) && (m_run != -INFINITY) && !first;
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = fast_exp2(m_run - m_use);
+            float psum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float p0 = fast_exp2(s[2 * c] - m_use);
+              const float p1 = fast_exp2(s[2 * c + 1] - m_use);
+              psum += p0 + p1;
+              pk[c] = f32x2_to_bf16x2(p0, p1);
+            }
+            l_run = l_run * alpha + psum;
+            m_run = m_new;
+            misc->alpha[st][row] = need ? alpha : 1.0f;
+            // P^T row `row`: 64 bf16 along KV, K-major 128-B swizzled
+            fence_proxy_async_smem();
+            const uint32_t pa = C::parea(sb, st) + row * 128;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+              st_shared_v4(pa + ((c8 ^ (row & 7)) << 4),
+                           make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]));
+          }
+          if (TMA_KV && !sparse) {
+            // rows past L in this tile may hold stale or non-finite bytes: zero their V part
+            int nvalid = L - j * kBlockRows;
+            nvalid = nvalid < 0 ? 0 : nvalid;
+            if (nvalid < kBlockRows) {
+              if (!row_thread && !mbar_wait(bar(kKvFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+              const uint32_t vs = C::stage(sb, st);
+              const int nz = (kBlockRows - nvalid) * 8 * 8;  // rows x slabs x 16-B chunks
+              for (int idx = wt; idx < nz; idx += 128) {
+                const int rr = nvalid + idx / 64;
+                const int sl = (idx / 8) & 7;
+                const int ch = idx & 7;
+                st_shared_v4(vs + sl * kSlab + rr * 128 + ch * 16, make_uint4(0, 0, 0, 0));
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          const bool any_need = named_bar_or(1, 128, need);
+          if (any_need) {
+            if (!mbar_wait(bar(kPvDone), (itj - 1) & 1, abort_flag, P.status)) return;
+            tc_fence_after();
+            for (int blk = 0; blk < 4; ++blk) {
+              for (int c = 0; c < nq; c += 16) {
+                uint32_t t16[16];
+                const uint32_t ta = tmem_o + lane_off + blk * 64 + c;
+                tmem_ld16(ta, t16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) t16[i] = __float_as_uint(__uint_as_float(t16[i]) * misc->alpha[st][c + i]);
+                tmem_st16(ta, t16);
+              }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+          }
+          mbar_arrive(bar(kPFull + st));
+        }
+        // -------------------------------------------------------- epilogue
+        const int base_split = P.num_splits[r];
+        const int nsplit = P.num_splits[r + 1] - base_split;
+        const int sg = base_split + sidx;
+        if (row_thread) {
+          float inv = 0.f, lse2 = -INFINITY;
+          if (l_run > 0.f) {
+            float denom = l_run;
+            if (nsplit == 1 && P.sink != nullptr) {
+              const int n = grow % P.heads;
+              denom += fast_exp2(P.sink[n] * 1.4426950408889634f - m_run);
+            }
+            inv = 1.0f / denom;
+            lse2 = m_run + log2f(l_run);
+          }
+          misc->inv[row] = inv;
+          misc->lse2[row] = lse2;
+          if (valid_row) {
+            const float lse_nat = lse2 * 0.6931471805599453f;
+            if (nsplit == 1) P.lse[(int64_t)r * R + grow] = lse_nat;
+            else P.part_lse[(int64_t)sg * R + grow] = lse_nat;
+          }
+        }
+        named_bar_sync(1, 128);
+        if (!mbar_wait(bar(kOFull), u & 1, abort_flag, P.status)) return;
+        tc_fence_after();
+        for (int blk = 0; blk < 4; ++blk) {
+          const int d = blk * 128 + wt;
+          for (int c = 0; c < nq; c += 16) {
+            uint32_t t16[16];
+            tmem_ld16(tmem_o + lane_off + blk * 64 + c, t16);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int qr = c + i;
+              if (qr >= rows_g) break;
+              const float v = __uint_as_float(t16[i]) * misc->inv[qr];
+              const int64_t flat = (int64_t)r * R + g * kGroupRows + qr;
+              if (nsplit == 1) {
+                const uint32_t b = f32x2_to_bf16x2(v, 0.f);
+                P.out[flat * 512 + d] = static_cast<uint16_t>(b & 0xFFFFu);
+              } else {
+                P.part_out[((int64_t)sg * R + g * kGroupRows + qr) * 512 + d] = v;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(kOFree));
+        it += ntile;
+        ++u;
+      });
+    }
+  } else if (warp >= 8 && !TMA_KV) {
+    // ------------------------------------------------------------ converters
+    const int ct = tid - 256;        // 0..255
+    const int crow = ct >> 2;        // tile row handled
+    const int part4 = ct & 3;        // chunk phase
+    int it = 0;
+    for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
+      const int part = w / G, g = w % G;
+      for_each_unit(P, part, [&](int r, int lo, int hi, int) {
+        if (*abort_flag) return;
+        const int L = P.seqlens[r];
+        const int tok = r * P.sq + (g * kGroupRows) / P.heads;   // sparse: the group's token
+        for (int j = lo; j < hi; ++j, ++it) {
+          const int st = it & 1;
+          if (it >= 2 && !mbar_wait(bar(kKvEmpty + st), ((it >> 1) - 1) & 1, abort_flag, P.status)) return;
+          fence_proxy_async_smem();
+          int pos;
+          bool valid;
+          if (sparse) {
+            const int kk = j * kBlockRows + crow;
+            pos = kk < P.topk ? P.indices[(int64_t)tok * P.topk + kk] : -1;
+            valid = pos >= 0 && pos < L;
+          } else {
+            pos = j * kBlockRows + crow;
+            valid = pos < L;
+          }
+          const uint8_t* rowp = nullptr;
+          const uint8_t* scp = nullptr;
+          if (valid) {
+            const int pi = pos >> P.log2_ps;
+            const int page = pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1;
+            if (page < 0 || page >= P.num_pages) {
+              if (part4 == 0) atomicOr(P.status, 2u);
+              valid = false;
+            } else {
+              const int off = pos & (P.page_size - 1);
+              rowp = P.kv + (int64_t)page * P.page_bytes + (int64_t)off * P.row_bytes;
+              scp = P.kv + (int64_t)page * P.page_bytes + (int64_t)P.page_size * P.row_bytes + off * 8;
+            }
+          }
+          const unsigned bal = __ballot_sync(0xffffffffu, valid && part4 == 0);
+          if (lane == 0) {
+            uint32_t byte = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) byte |= ((bal >> (4 * k)) & 1u) << k;
+            misc->mask[st][(ct >> 5)] = static_cast<uint8_t>(byte);
+          }
+          constexpr int CPT = C::kChunksPerThread;
+          uint4 v[CPT];
+#pragma unroll
+          for (int i = 0; i < CPT; ++i) {
+            const int c = part4 + 4 * i;
+            v[i] = valid ? ld_nc_v4(rowp + c * 16) : make_uint4(0, 0, 0, 0);
+          }
+          uint2 sc = make_uint2(0, 0);
+          if (LAYOUT != 0 && valid) sc = ld_nc_v2(scp);
+          const uint32_t dst = C::stage(sb, st);
+#pragma unroll
+          for (int i = 0; i < CPT; ++i) {
+            const int c = part4 + 4 * i;
+            if (LAYOUT == 0) {
+              // bf16 copy: chunk c = dims [8c, 8c + 8)
+              st_shared_v4(dst + (c >> 3) * kSlab + sw128_offset(crow, (c & 7) * 8), v[i]);
+            } else if (c < C::kNope / 16) {
+              // 16 e4m3 codes of group c/4 -> 16 bf16 at dims [16c, 16c + 16)
+              const int grp = c >> 2;
+              const uint32_t sbyte = (grp < 4 ? (sc.x >> (8 * grp)) : (sc.y >> (8 * (grp - 4)))) & 0xFFu;
+              const float scale = valid ? ue8m0_to_f32(sbyte) : 0.f;
+              const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+              uint32_t o[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 a = e4m3x2_to_f32x2(w4[q] & 0xFFFFu);
+                const float2 b = e4m3x2_to_f32x2(w4[q] >> 16);
+                o[2 * q] = f32x2_to_bf16x2(a.x * scale, a.y * scale);
+                o[2 * q + 1] = f32x2_to_bf16x2(b.x * scale, b.y * scale);
+              }
+              const uint32_t sl = dst + grp * kSlab;
+              const int k0 = (c & 3) * 16;
+              st_shared_v4(sl + sw128_offset(crow, k0), make_uint4(o[0], o[1], o[2], o[3]));
+              st_shared_v4(sl + sw128_offset(crow, k0 + 8), make_uint4(o[4], o[5], o[6], o[7]));
+            } else {
+              // RoPE: 8 bf16 at dims [nope + 8k, nope + 8k + 8)
+              const int dim = C::kNope + 8 * (c - C::kNope / 16);
+              st_shared_v4(dst + (dim >> 6) * kSlab + sw128_offset(crow, dim & 63), v[i]);
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kKvFull + st));
+        }
+      });
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(DecodeVariant v) {
+  switch (v) {
+    case DecodeVariant::kBf16Tma: return Cfg<0, true>::kSmem;
+    case DecodeVariant::kBf16Gather: return Cfg<0, false>::kSmem;
+    case DecodeVariant::kFp8_448: return Cfg<1, false>::kSmem;
+    case DecodeVariant::kFp8_512: return Cfg<2, false>::kSmem;
+  }
+  return 0;
+}
+
+template <int LAYOUT, bool TMA_KV>
+static cudaError_t launch_variant(const DecodeParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map, int grid,
+                                  cudaStream_t stream) {
+  auto kern = mla_decode_kernel<LAYOUT, TMA_KV>;
+  const size_t smem = Cfg<LAYOUT, TMA_KV>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kDecodeThreads, smem, stream>>>(p, q_map, kv_map);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(DecodeVariant v, const DecodeParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+                          int grid, cudaStream_t stream) {
+  switch (v) {
+    case DecodeVariant::kBf16Tma: return launch_variant<0, true>(p, q_map, kv_map, grid, stream);
+    case DecodeVariant::kBf16Gather: return launch_variant<0, false>(p, q_map, kv_map, grid, stream);
+    case DecodeVariant::kFp8_448: return launch_variant<1, false>(p, q_map, kv_map, grid, stream);
+    case DecodeVariant::kFp8_512: return launch_variant<2, false>(p, q_map, kv_map, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mla

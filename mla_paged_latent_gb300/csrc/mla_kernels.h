@@ -1,0 +1,76 @@
+// Internal interface between the C-ABI layer (api.cpp) and the CUDA kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+constexpr int kBlockRows = 64;    // KV rows per tile
+constexpr int kGroupRows = 64;    // query rows per work item
+constexpr int kDecodeThreads = 512;
+
+struct DecodeParams {
+  const uint8_t* kv;              // paged cache (used by the converter path)
+  const int32_t* block_table;     // [batch, max_pages]
+  const int32_t* seqlens;         // [batch]
+  const float* sink;              // [heads] or null
+  const int32_t* indices;         // [T, topk] or null
+  const int32_t* sched;           // [num_partitions, 8]
+  const int32_t* num_splits;      // [batch + 1]
+  uint16_t* out;                  // bf16 [T, heads, 512]
+  float* lse;                     // [T, heads]
+  float* part_out;                // [total_splits, R, 512]
+  float* part_lse;                // [total_splits, R]
+  unsigned int* status;           // device status word
+  int64_t num_pages;
+  int64_t page_bytes;
+  int32_t row_bytes;
+  int32_t page_size;
+  int32_t log2_ps;
+  int32_t max_pages;
+  int32_t batch;
+  int32_t sq;
+  int32_t heads;
+  int32_t rows_per_req;           // R = sq * heads
+  int32_t groups;                 // ceil(R / 64)
+  int32_t qbox_rows;              // rows of one Q TMA box = min(64, R)
+  int32_t topk;
+  int32_t causal;
+  int32_t num_partitions;
+  int32_t num_work;               // num_partitions * groups
+  float scale_log2;               // sm_scale * log2(e)
+};
+
+// Kernel variants: layout 0 with TMA page loads (dense), layout 0 gathered by
+// the converter warps (sparse), layouts 1 and 2 (fp8, dense or sparse).
+enum class DecodeVariant { kBf16Tma = 0, kBf16Gather = 1, kFp8_448 = 2, kFp8_512 = 3 };
+
+size_t decode_smem_bytes(DecodeVariant v);
+cudaError_t launch_decode(DecodeVariant v, const DecodeParams& p, const CUtensorMap& q_map,
+                          const CUtensorMap& kv_map, int grid, cudaStream_t stream);
+
+cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
+                           int rows_per_req, int heads, const float* sink, uint16_t* out, float* lse,
+                           cudaStream_t stream);
+
+cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout,
+                            int64_t num_pages, int page_size, int64_t page_bytes, cudaStream_t stream);
+
+cudaError_t launch_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
+                             const int32_t* bt_row, int max_pages, int length, float* out, cudaStream_t stream);
+
+// Host split-KV plan (rule documented on mla_decode_plan in include/mla_decode.h).
+struct PlanResult {
+  std::vector<int32_t> sched;        // [partitions * 8]
+  std::vector<int32_t> num_splits;   // [batch + 1]
+  int partitions = 0;
+  int groups = 0;
+  int total_splits = 0;
+  int max_splits = 0;
+};
+PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int topk, int min_splits, int num_sms);
+
+}  // namespace mla

@@ -1,0 +1,74 @@
+// Host split-KV planner.
+//
+// The pages fix the planner's inputs and outputs — cache_seqlens, query tokens
+// per request x heads and topk in; tile-scheduler metadata and per-request
+// split counts out ("Implementation:Sgl project Sglang Flash MLA", Signature
+// and I/O Contract of get_mla_metadata) — but not the rule. This file's rule:
+// requests are cut into KV blocks of 64 rows, each costing 1 plus a fixed 2 per
+// split; partitions (one per SM, or per SM group when a request needs several
+// query-row groups) are filled greedily in request order up to
+// ceil(total cost / partitions); a request that does not fit is split. The
+// include/mla_decode.h comment on mla_decode_plan states the rule in full.
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "mla_kernels.h"
+
+namespace mla {
+
+constexpr int kFixedCost = 2;
+
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int topk, int min_splits, int num_sms) {
+  PlanResult res;
+  const int groups = static_cast<int>(cdiv(static_cast<int64_t>(sq) * heads, kGroupRows));
+  const int parts = std::max(1, num_sms / groups);
+  std::vector<int> nb(batch);
+  int64_t total = 0;
+  int min_nb = 1 << 30;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t K = topk > 0 ? topk : std::max<int32_t>(seqlens[b], 0);
+    nb[b] = static_cast<int>(std::max<int64_t>(1, cdiv(K, kBlockRows)));
+    total += nb[b] + kFixedCost;
+    min_nb = std::min(min_nb, nb[b]);
+  }
+  int64_t payload = std::max<int64_t>(cdiv(total, parts), kFixedCost + 1);
+  if (min_splits > 1 && batch > 0) {
+    const int64_t cap = std::max(1, min_nb / min_splits);
+    payload = std::min<int64_t>(payload, cap + kFixedCost);
+  }
+  std::vector<int> splits(batch, 0);
+  int b = 0, blk = 0;
+  while (b < batch) {
+    int64_t budget = payload;
+    const int begin_b = b, begin_blk = blk, first_split = splits[b];
+    while (b < batch && budget > kFixedCost) {
+      const int64_t remain = nb[b] - blk;
+      const int64_t take = std::min<int64_t>(remain, budget - kFixedCost);
+      budget -= take + kFixedCost;
+      splits[b] += 1;
+      blk += static_cast<int>(take);
+      if (blk == nb[b]) {
+        ++b;
+        blk = 0;
+      } else {
+        break;
+      }
+    }
+    const int32_t row[8] = {begin_b, begin_blk, b, blk, first_split, 0, 0, 0};
+    res.sched.insert(res.sched.end(), row, row + 8);
+  }
+  res.num_splits.assign(batch + 1, 0);
+  for (int i = 0; i < batch; ++i) {
+    res.num_splits[i + 1] = res.num_splits[i] + splits[i];
+    res.max_splits = std::max(res.max_splits, splits[i]);
+  }
+  res.partitions = static_cast<int>(res.sched.size() / 8);
+  res.groups = groups;
+  res.total_splits = res.num_splits[batch];
+  return res;
+}
+
+}  // namespace mla

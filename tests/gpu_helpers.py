@@ -1,0 +1,106 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the binding
+(which calls the C ABI) and the oracle on the same seeded workload, and
+compare them within the stated tolerances."""
+import numpy as np
+import torch
+
+import mla_paged_latent_gb300 as mla
+import oracle
+
+# Tolerances of the decode outputs (benchmark spec; elementwise bound
+# relaxed to 1e-2 * max(1, |ref|) because one bf16 half-ulp exceeds 1e-2 once
+# |out| > 2).
+OUT_ABS = 1e-2
+OUT_REL_L2 = 5e-3
+LSE_ABS = 1e-3
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+class DeviceWorkload:
+    def __init__(self, w):
+        self.w = w
+        c = w.cfg
+        self.q = bf16_tensor(w.q)
+        self.kv = torch.from_numpy(w.kv_cache).cuda()
+        self.bt = torch.from_numpy(w.block_table).cuda()
+        self.sl = torch.from_numpy(w.seqlens).cuda()
+        self.sink = None if w.sink is None else torch.from_numpy(w.sink).cuda()
+        self.idx = None if w.indices is None else torch.from_numpy(w.indices).cuda()
+        self.rows = None if w.new_rows is None else bf16_tensor(w.new_rows)
+        self.slots = None if w.new_slots is None else torch.from_numpy(w.new_slots).cuda()
+        T, N = w.q.shape[0], w.q.shape[1]
+        self.out = torch.empty(T, N, 512, dtype=torch.bfloat16, device="cuda")
+        self.lse = torch.empty(T, N, dtype=torch.float32, device="cuda")
+        self.plan = None
+
+    def kv_write(self):
+        c = self.w.cfg
+        if self.rows is not None:
+            mla.mla_kv_write(self.rows, self.slots, self.kv, c.layout, c.page_size)
+
+    def make_plan(self, num_sms=None, min_splits=None):
+        c = self.w.cfg
+        ms = c.min_splits if min_splits is None else min_splits
+        self.plan = mla.mla_decode_plan(self.w.seqlens, c.sq, c.heads, c.topk, ms, num_sms)
+        self.sched = torch.from_numpy(self.plan.sched).cuda()
+        self.ns = torch.from_numpy(self.plan.num_splits).cuda()
+        self.ws = mla.alloc_workspace(self.plan.workspace_bytes)
+        return self.plan
+
+    def decode(self):
+        c = self.w.cfg
+        p = self.plan
+        mla.mla_decode(self.q, self.kv, c.layout, c.page_size, self.bt, self.sl, c.sq, c.sm_scale, self.sched,
+                       self.ns, p.num_partitions, p.total_splits, self.ws, self.out, self.lse, sink=self.sink,
+                       indices=self.idx, causal=c.causal)
+
+    def run(self, num_sms=None, min_splits=None, write=True):
+        if write:
+            self.kv_write()
+        self.make_plan(num_sms, min_splits)
+        self.decode()
+        assert mla.mla_read_status(self.ws) == 0
+        torch.cuda.synchronize()
+        return bf16_to_f64(self.out), self.lse.cpu().numpy().astype(np.float64)
+
+
+def oracle_cache(w, write=True):
+    c = w.cfg
+    if write and w.new_rows is not None:
+        return oracle.kv_write(w.new_rows, w.new_slots, w.kv_cache, c.layout, c.page_size)
+    return w.kv_cache
+
+
+def oracle_decode(w, kv=None, select=None):
+    c = w.cfg
+    kv = oracle_cache(w) if kv is None else kv
+    return oracle.mla_decode(w.q, kv, c.layout, c.page_size, w.block_table, w.seqlens, c.sq, c.sm_scale,
+                             sink=w.sink, indices=w.indices, causal=c.causal, select=select)
+
+
+def assert_close(out, lse, ref_out, ref_lse, what=""):
+    out = np.asarray(out, dtype=np.float64)
+    ref_out = np.asarray(ref_out, dtype=np.float64)
+    assert np.all(np.isfinite(out)), f"{what}: non-finite output"
+    err = np.abs(out - ref_out)
+    bound = OUT_ABS * np.maximum(1.0, np.abs(ref_out))
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), f"{what}: max abs err {err.max():.3g} (at {worst}: {out[worst]} vs {ref_out[worst]})"
+    nref = np.linalg.norm(ref_out)
+    if nref > 0:
+        rel = np.linalg.norm(out - ref_out) / nref
+        assert rel <= OUT_REL_L2, f"{what}: rel L2 {rel:.3g}"
+    inf_ref = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), inf_ref), f"{what}: -inf lse pattern differs"
+    if (~inf_ref).any():
+        lerr = np.abs(lse[~inf_ref] - ref_lse[~inf_ref]).max()
+        assert lerr <= LSE_ABS, f"{what}: lse abs err {lerr:.3g}"
+    assert np.all(out[inf_ref] == 0), f"{what}: empty rows must be zero"
+    return float(err.max())

@@ -1,0 +1,211 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element by
+element, on seeded workloads shaped like the decode configurations, at sizes
+the oracle finishes in seconds that still span several tiles and ragged tails;
+plus the edge cases the method has. Bit-exact where the result is integer or
+byte work (KV-row write, page gather); within the stated tolerances otherwise."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_paged_latent_gb300 as mla
+import oracle
+import workloads
+from gpu_helpers import DeviceWorkload, assert_close, bf16_tensor, oracle_cache, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from mla_paged_latent_gb300 import build
+    build.build()
+    mla.load()
+
+
+# ----------------------------------------------------------------------------- KV write / gather (bit-exact)
+@pytest.mark.parametrize("layout", [0, 1, 2])
+def test_kv_write_bit_exact(layout):
+    rng = np.random.default_rng(20 + layout)
+    ps = 16
+    pb = workloads.page_bytes(layout, ps)
+    num_pages = 9
+    kv0 = rng.integers(0, 256, (num_pages, pb), dtype=np.uint8)
+    n = 70
+    re = workloads.row_elems(layout)
+    x = (rng.standard_normal((n, re)) * 2.0 ** rng.integers(-30, 30, (n, 1))).astype(np.float32)
+    x[0, :64] = 0.0
+    x[1, 64:128] = -0.0
+    x[2, :] = 1e-12
+    x[3, :64] = 448.0
+    x[4, :64] = np.linspace(-1000, 1000, 64)
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    slots = rng.permutation(num_pages * ps)[:n].astype(np.int32)
+    slots[5] = -1
+    ref = oracle.kv_write(bits, slots, kv0, layout, ps)
+    kv = torch.from_numpy(kv0).cuda()
+    mla.mla_kv_write(bf16_tensor(bits), torch.from_numpy(slots).cuda(), kv, layout, ps)
+    got = kv.cpu().numpy()
+    diff = np.argwhere(got != ref)
+    assert diff.size == 0, f"{len(diff)} bytes differ, first at {diff[:5].tolist()}"
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+def test_kv_gather_bit_exact(layout):
+    cfg = workloads.dsv4(batch=2, seqlens=(77, 150), len_dist="fixed", page_size=16, layout=layout)
+    w = workloads.generate(cfg)
+    kv = torch.from_numpy(w.kv_cache).cuda()
+    for b in range(2):
+        L = int(w.seqlens[b])
+        out = torch.empty(L, workloads._DQK[layout], dtype=torch.float32, device="cuda")
+        mla.mla_kv_gather(kv, layout, 16, torch.from_numpy(w.block_table[b]).cuda(), L, out)
+        ref = oracle.kv_gather(w.kv_cache, layout, 16, w.block_table[b], L)
+        assert np.array_equal(out.cpu().numpy().astype(np.float64), ref)
+
+
+# ----------------------------------------------------------------------------- combine
+def test_combine_matches_oracle():
+    rng = np.random.default_rng(30)
+    B, N, sq = 3, 16, 2
+    R = sq * N
+    nsplit = [3, 1, 5]
+    ns = np.concatenate([[0], np.cumsum(nsplit)]).astype(np.int32)
+    S = int(ns[-1])
+    q = rng.standard_normal((B, R, 576))
+    part_out = np.zeros((S, R, 512))
+    part_lse = np.zeros((S, R))
+    ref_out = np.zeros((B, R, 512))
+    ref_lse = np.zeros((B, R))
+    sink = rng.standard_normal(N).astype(np.float32)
+    for b in range(B):
+        for r in range(R):
+            rows = rng.standard_normal((int(rng.integers(0, 40)) * nsplit[b] + 1, 576))
+            cuts = np.sort(rng.integers(0, rows.shape[0] + 1, nsplit[b] - 1))
+            cuts = np.concatenate([[0], cuts, [rows.shape[0]]])
+            for s in range(nsplit[b]):
+                o, l = oracle.attend(q[b, r], rows[cuts[s]:cuts[s + 1]], 512, 0.05)
+                part_out[ns[b] + s, r] = o
+                part_lse[ns[b] + s, r] = l
+            ref_out[b, r], ref_lse[b, r] = oracle.combine(part_out[ns[b]:ns[b + 1], r], part_lse[ns[b]:ns[b + 1], r],
+                                                          sink=float(sink[r % N]))
+    out = torch.zeros(B, R, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(B, R, dtype=torch.float32, device="cuda")
+    mla.mla_combine(torch.from_numpy(part_out.astype(np.float32)).cuda(),
+                    torch.from_numpy(part_lse.astype(np.float32)).cuda(), torch.from_numpy(ns).cuda(), R, N, out, lse,
+                    sink=torch.from_numpy(sink).cuda())
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    for b in (0, 2):
+        assert_close(o[b], l[b], ref_out[b], ref_lse[b], f"combine request {b}")
+    assert np.all(o[1] == 0) and np.all(l[1] == 0)  # single-split request untouched
+
+
+# ----------------------------------------------------------------------------- decode parity, small shapes
+SMALL = {
+    "tiny": lambda: workloads.tiny(),
+    "dsv3_small": lambda: workloads.dsv3(batch=6, seqlens=(1, 63, 64, 65, 1000, 3001), len_dist="fixed"),
+    "dsv4_small": lambda: workloads.dsv4(batch=5, seqlens=(1, 100, 129, 700, 2500), len_dist="fixed"),
+    "verify_small": lambda: workloads.verify(batch=3, seqlens=(9, 204, 1004), len_dist="fixed"),
+    "sparse_small": lambda: workloads.sparse(batch=3, seqlens=(5000, 300, 7000), topk=300, len_dist="fixed"),
+    "dsv3_ps16": lambda: workloads.dsv3(batch=3, seqlens=(37, 130, 700), len_dist="fixed", page_size=16),
+    "dsv4_ps256": lambda: workloads.dsv4(batch=3, seqlens=(300, 513, 1500), len_dist="fixed", page_size=256),
+    "bf16_sparse": lambda: workloads.dsv3(batch=2, seqlens=(900, 2000), len_dist="fixed", topk=200, pad_frac=0.1),
+    "fp8_448_sparse": lambda: workloads.dsv4(batch=2, seqlens=(900, 2000), len_dist="fixed", topk=130, pad_frac=0.1),
+    "fp8_512_dense": lambda: workloads.sparse(batch=3, seqlens=(64, 500, 1200), topk=0, min_splits=1, len_dist="fixed"),
+    "verify_heads16": lambda: workloads.verify(batch=3, heads=16, seqlens=(4, 70, 300), len_dist="fixed"),
+    "tail_nan_bf16": lambda: workloads.dsv3(batch=3, seqlens=(10, 70, 200), len_dist="fixed", tail_fill="nan"),
+    "tail_nan_fp8": lambda: workloads.dsv4(batch=3, seqlens=(10, 70, 200), len_dist="fixed", tail_fill="nan"),
+    "empty_requests": lambda: workloads.dsv4(batch=4, seqlens=(0, 65, 0, 3), len_dist="fixed", new_rows=False),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_decode_small(name):
+    w = workloads.generate(SMALL[name]())
+    d = DeviceWorkload(w)
+    out, lse = d.run()
+    if w.new_rows is not None:
+        assert np.array_equal(d.kv.cpu().numpy(), oracle_cache(w)), "kv_write bytes differ"
+    ref_out, ref_lse = oracle_decode(w)
+    assert_close(out, lse, ref_out, ref_lse, name)
+
+
+@pytest.mark.parametrize("name", ["dsv3_small", "dsv4_small", "verify_small", "sparse_small"])
+@pytest.mark.parametrize("num_sms", [1, 7, 40])
+def test_decode_forced_splits(name, num_sms):
+    """Few partitions -> long partitions; many partitions -> many splits merged
+    by the combine. Every plan must give the same result."""
+    w = workloads.generate(SMALL[name]())
+    d = DeviceWorkload(w)
+    d.kv_write()
+    ref_out, ref_lse = oracle_decode(w)
+    groups = -(-w.cfg.sq * w.cfg.heads // 64)
+    for ms in (1, 6):
+        d.make_plan(num_sms=num_sms * groups, min_splits=ms)
+        d.decode()
+        assert mla.mla_read_status(d.ws) == 0
+        out = d.out.float().cpu().numpy().astype(np.float64)
+        lse = d.lse.cpu().numpy().astype(np.float64)
+        assert_close(out, lse, ref_out, ref_lse, f"{name} sms={num_sms} min_splits={ms} splits={d.plan.total_splits}")
+
+
+def test_decode_deterministic():
+    w = workloads.generate(SMALL["dsv3_small"]())
+    d = DeviceWorkload(w)
+    a, la = d.run()
+    d.decode()
+    torch.cuda.synchronize()
+    b = d.out.float().cpu().numpy()
+    assert np.array_equal(a, b) and np.array_equal(la, d.lse.cpu().numpy())
+
+
+def test_large_score_growth_triggers_rescale():
+    """Scores that grow along the sequence force the lazy O rescale (running max
+    rising by more than 2^8 between tiles)."""
+    cfg = workloads.dsv3(batch=2, heads=64, seqlens=(640, 1000), len_dist="fixed", new_rows=False)
+    w = workloads.generate(cfg)
+    # scale the RoPE part of KV rows up with position so that later tiles dominate
+    ps = cfg.page_size
+    kv = w.kv_cache.copy()
+    for b in range(2):
+        for j in range(int(w.seqlens[b])):
+            page = w.block_table[b, j // ps]
+            off = (j % ps) * 1152
+            row = kv[page, off:off + 1152].view(np.uint16).copy()
+            vals = torch.from_numpy(row.view(np.int16).copy()).view(torch.bfloat16).float()
+            vals[512:] = vals[512:] * (1 + j / 40.0)
+            kv[page, off:off + 1152] = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint8)
+    w.kv_cache = kv
+    w.q[:, :, 512:] = torch.full((1,), 2.0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)[0]
+    d = DeviceWorkload(w)
+    out, lse = d.run()
+    ref_out, ref_lse = oracle_decode(w)
+    assert_close(out, lse, ref_out, ref_lse, "rescale")
+
+
+def test_causal_with_short_context():
+    """Draft tokens whose visible prefix is empty (L < s_q) give zero output and -inf lse."""
+    cfg = workloads.verify(batch=2, heads=64, seqlens=(2, 6), len_dist="fixed")
+    w = workloads.generate(cfg)
+    d = DeviceWorkload(w)
+    out, lse = d.run()
+    ref_out, ref_lse = oracle_decode(w)
+    assert np.isneginf(ref_lse[0]).all() and np.isneginf(ref_lse[1]).all()
+    assert_close(out, lse, ref_out, ref_lse, "short causal")
+
+
+def test_bad_page_is_reported_not_read():
+    cfg = workloads.dsv3(batch=2, heads=64, seqlens=(100, 200), len_dist="fixed", new_rows=False)
+    w = workloads.generate(cfg)
+    w.block_table[1, 1] = 10_000_000   # out of range for a row < L
+    d = DeviceWorkload(w)
+    d.make_plan()
+    d.decode()
+    with pytest.raises(mla.MlaError):
+        mla.mla_read_status(d.ws)
+    ref_out, ref_lse = oracle_decode(workloads.generate(cfg), kv=w.kv_cache)
+    out = d.out.float().cpu().numpy().astype(np.float64)
+    # the other request is unaffected
+    assert_close(out[:1], d.lse.cpu().numpy()[:1].astype(np.float64), ref_out[:1], ref_lse[:1], "good request")
