@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-latent MLA decode hot path on GB300.
+
+One step = one pass of the whole path over one batch: mla_kv_write of the
+batch's new rows, then mla_decode (persistent decode kernel) and, for requests
+the plan split, mla_combine. Inputs are resident in HBM when the timed region
+starts; L2 is flushed (a 256 MiB buffer is overwritten) between steps, outside
+each step's CUDA-event pair.
+
+Default workload (N=1): the DeepSeek-V3-shaped bf16 decode batch — 64 requests
+x 1 token, 128 heads, bf16 latent KV rows [512 | 64], context lengths
+U{1024..8192}, page 64, seed 0. Other workloads: --config dsv4|verify|sparse|tiny.
+
+Under torchrun (N > 1) every rank runs its own replica (the decode shards by
+request and needs no collective); timings are max-reduced over ranks.
+
+--impl reference times the oracle (plain fp64 C, OpenMP) on this machine's
+host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode query-tokens/s, KV GB/s and % of roofline on 1 GB300"
+UNIT = "query-tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_cost(w):
+    """Bytes and MMA FLOPs one decode launch must move / perform (per the scope
+    table): every candidate KV row once (row + its scale slot for fp8), q, out,
+    lse (and the sparse index list)."""
+    c = w.cfg
+    T, N = w.q.shape[0], c.heads
+    row_b = {0: 1152, 1: 576 + 8, 2: 640 + 8}[c.layout]
+    dqk = {0: 576, 1: 512, 2: 576}[c.layout]
+    if w.indices is not None:
+        L = np.repeat(w.seqlens, c.sq)[:, None]
+        rows_per_token = ((w.indices >= 0) & (w.indices < L)).sum(axis=1)
+        kv_rows = int(rows_per_token.sum())          # rows gathered per token (tokens do not share rows)
+        scored = int(rows_per_token.sum()) * N
+        extra = w.indices.nbytes
+    else:
+        kv_rows = int(w.seqlens.sum())
+        if c.causal:
+            scored = 0
+            for b in range(c.batch):
+                L = int(w.seqlens[b])
+                for i in range(c.sq):
+                    scored += max(0, min(L, L - c.sq + i + 1)) * N
+        else:
+            scored = kv_rows * N * c.sq
+        extra = 0
+    kv_bytes = kv_rows * row_b
+    q_bytes = T * N * dqk * 2
+    out_bytes = T * N * 512 * 2 + T * N * 4
+    flops = 2.0 * scored * (dqk + 512)
+    return dict(kv_bytes=kv_bytes, bytes=kv_bytes + q_bytes + out_bytes + extra, flops=flops, kv_rows=kv_rows)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for k, name in enumerate(names):
+                    if parts[5 + k].lower() == "active":
+                        reasons.add(name)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "mla_paged_latent_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_name):
+    """Per-launch DRAM bytes of the decode kernel from a committed ncu summary,
+    valid only while the kernel sources are unchanged."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(config_name)
+        if e and e.get("source_hash") == source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def run_reference(args, rank, world):
+    import oracle
+    import workloads
+    if rank != 0:
+        return
+    w = workloads.generate(workloads.CONFIGS[args.config]())
+    c = w.cfg
+    oracle.build()
+    T, N = w.q.shape[0], c.heads
+    # each step: one head for each of `npairs` distinct tokens, (one oracle call)
+    cores = os.cpu_count() or 1
+    npairs = min(T, cores)
+    kv = oracle.kv_write(w.new_rows, w.new_slots, w.kv_cache, c.layout, c.page_size) if w.new_rows is not None \
+        else w.kv_cache
+    step_times = []
+    for s in range(args.warmup + args.steps):
+        toks = (np.arange(npairs) + s * npairs) % T
+        heads = (s * 7 + np.arange(npairs)) % N
+        t0 = time.perf_counter()
+        oracle.mla_decode(w.q, kv, c.layout, c.page_size, w.block_table, w.seqlens, c.sq, c.sm_scale, sink=w.sink,
+                          indices=w.indices, causal=c.causal, select=(toks.astype(np.int32), heads.astype(np.int32)))
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            step_times.append(dt)
+    total = sum(step_times)
+    tokens = len(step_times) * npairs / N
+    value = tokens / total
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / len(step_times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": config_dict(w, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, npairs), "kind": "oracle",
+                             "sample": f"per step {npairs} (token, head) pairs of the {args.config} batch "
+                                       f"({npairs}/{N} query-tokens), fp64 oracle, OpenMP over tokens"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, args):
+    c = w.cfg
+    desc = {
+        "dsv3": "DSV3-shaped bf16 decode: 64 x 1 token, 128 heads, bf16 KV [512|64], L~U{1024..8192}, page 64",
+        "dsv4": "DSV4-shaped fp8 decode: 128 x 1 token, 64 heads, fp8-448+ue8m0/64 KV, L log-uniform [512,32768], "
+                "page 64, sink",
+        "verify": "speculative verify: 32 x 4 draft tokens (causal), 128 heads, bf16 KV, context U{2048..16384}+4, "
+                  "page 64, mla_kv_write of the 128 new rows",
+        "sparse": "sparse top-k decode: 64 x 1 token, 128 heads, fp8-512+ue8m0/64 KV, L=65536, topk 2048 (10% -1), "
+                  "page 64, >= 4 splits",
+        "tiny": "tiny decode: 2 x 1 token, 16 heads, bf16 KV, L=(37,130), page 16",
+    }[args.config]
+    return {"workload": desc, "batch": c.batch, "q_tokens_per_req": c.sq, "heads": c.heads,
+            "kv_layout": ["bf16-576", "fp8-448-ue8m0", "fp8-512-ue8m0"][c.layout], "page_size": c.page_size,
+            "kv_rows": int(w.seqlens.sum()), "seed": c.seed, "l2": "flushed between steps (256 MiB write)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="dsv3", choices=["dsv3", "dsv4", "verify", "sparse", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    import torch
+
+    import mla_paged_latent_gb300 as mla
+    import workloads
+    from mla_paged_latent_gb300 import build as mla_build
+
+    if rank == 0 or world == 1:
+        mla_build.build()
+    if dist is not None:
+        dist.barrier()
+    mla.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workloads.generate(workloads.CONFIGS[args.config](seed=0))
+    c = w.cfg
+    T, N = w.q.shape[0], c.heads
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q = bf16(w.q)
+    kv = torch.from_numpy(w.kv_cache).to(dev)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    sl = torch.from_numpy(w.seqlens).to(dev)
+    sink = None if w.sink is None else torch.from_numpy(w.sink).to(dev)
+    idx = None if w.indices is None else torch.from_numpy(w.indices).to(dev)
+    rows = None if w.new_rows is None else bf16(w.new_rows)
+    slots = None if w.new_slots is None else torch.from_numpy(w.new_slots).to(dev)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan = mla.mla_decode_plan(w.seqlens, c.sq, N, c.topk, c.min_splits, num_sms)
+    sched = torch.from_numpy(plan.sched).to(dev)
+    ns = torch.from_numpy(plan.num_splits).to(dev)
+    ws = mla.alloc_workspace(plan.workspace_bytes, dev)
+    out = torch.empty(T, N, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, N, dtype=torch.float32, device=dev)
+    part_out, part_lse = mla.workspace_partials(ws, plan.total_splits, c.sq * N)
+    split = plan.total_splits > c.batch
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        if rows is not None:
+            mla.mla_kv_write(rows, slots, kv, c.layout, c.page_size, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        mla.mla_decode(q, kv, c.layout, c.page_size, bt, sl, c.sq, c.sm_scale, sched, ns, plan.num_partitions,
+                       plan.total_splits, ws, out, lse, sink=sink, indices=idx, causal=c.causal, skip_combine=True,
+                       stream=stream)
+        if evs:
+            evs[2].record(stream)
+        if split:
+            mla.mla_combine(part_out, part_lse, ns, c.sq * N, N, out, lse, sink=sink, stream=stream)
+        if evs:
+            evs[3].record(stream)
+
+    launches_per_step = (1 if rows is not None else 0) + 1 + (1 if split else 0)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    mla.mla_read_status(ws)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.15)
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        step(events[k])
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    mla.mla_read_status(ws)
+    step_ms = [e[0].elapsed_time(e[3]) for e in events]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in events]
+    kvw_ms = [e[0].elapsed_time(e[1]) for e in events]
+    cmb_ms = [e[2].elapsed_time(e[3]) for e in events]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * T / (ms_per_step * 1e-3)
+
+    # ---- e2e through the public API with host buffers (pinned), copies inside the timed region
+    hq = torch.from_numpy(w.q.view(np.int16)).pin_memory()
+    hrows = None if w.new_rows is None else torch.from_numpy(w.new_rows.view(np.int16)).pin_memory()
+    hslots = None if w.new_slots is None else torch.from_numpy(w.new_slots).pin_memory()
+    hbt = torch.from_numpy(w.block_table).pin_memory()
+    hsl = torch.from_numpy(w.seqlens).pin_memory()
+    hidx = None if w.indices is None else torch.from_numpy(w.indices).pin_memory()
+    hout = torch.empty(T, N, 512, dtype=torch.int16).pin_memory()
+    hlse = torch.empty(T, N, dtype=torch.float32).pin_memory()
+    dq = torch.empty_like(q)
+    drows = None if rows is None else torch.empty_like(rows)
+    dslots = None if slots is None else torch.empty_like(slots)
+    dbt, dsl = torch.empty_like(bt), torch.empty_like(sl)
+    didx = None if idx is None else torch.empty_like(idx)
+
+    def e2e_step():
+        dq.view(torch.int16).copy_(hq, non_blocking=True)
+        if drows is not None:
+            drows.view(torch.int16).copy_(hrows, non_blocking=True)
+            dslots.copy_(hslots, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dsl.copy_(hsl, non_blocking=True)
+        if didx is not None:
+            didx.copy_(hidx, non_blocking=True)
+        p = mla.mla_decode_plan(w.seqlens, c.sq, N, c.topk, c.min_splits, num_sms)
+        hs = torch.from_numpy(p.sched).pin_memory()
+        hn = torch.from_numpy(p.num_splits).pin_memory()
+        dsch = hs.to(dev, non_blocking=True)
+        dns = hn.to(dev, non_blocking=True)
+        if drows is not None:
+            mla.mla_kv_write(drows, dslots, kv, c.layout, c.page_size, stream=stream)
+        mla.mla_decode(dq, kv, c.layout, c.page_size, dbt, dsl, c.sq, c.sm_scale, dsch, dns, p.num_partitions,
+                       p.total_splits, ws, out, lse, sink=sink, indices=didx, causal=c.causal, stream=stream)
+        hout.copy_(out.view(torch.int16), non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        return hs.nbytes + hn.nbytes
+
+    for _ in range(5):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    sched_bytes = 0
+    for _ in range(args.e2e_steps):
+        sched_bytes = e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = (w.q.nbytes + (0 if w.new_rows is None else w.new_rows.nbytes + w.new_slots.nbytes) +
+           w.block_table.nbytes + w.seqlens.nbytes + (0 if w.indices is None else w.indices.nbytes) + sched_bytes)
+    d2h = T * N * 512 * 2 + T * N * 4
+    e2e_value = world * T * args.e2e_steps / e2e_s
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    cost = algorithmic_cost(w)
+    dec_avg_s = statistics.mean(dec_ms) * 1e-3
+    t_hbm = cost["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = cost["flops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = cost["bytes"] / dec_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    else:
+        achieved = cost["flops"] / dec_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"]}
+    traffic = recorded_traffic(args.config)
+    roof.update({"traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src ==
+                 "measured" else "fallback", "kernel": "mla_decode_kernel", "alg_bytes_per_launch": cost["bytes"],
+                 "alg_flops_per_launch": cost["flops"], "kernel_ms": statistics.mean(dec_ms),
+                 "step_frac_of_roofline": max(t_hbm, t_tc) / (ms_per_step * 1e-3)})
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        t0 = time.perf_counter()
+        kv_o = oracle.kv_write(w.new_rows, w.new_slots, w.kv_cache, c.layout, c.page_size) \
+            if w.new_rows is not None else w.kv_cache
+        if args.config in ("dsv3", "tiny", "dsv4"):
+            toks = np.arange(T)
+        else:
+            toks = np.arange(min(T, 32))
+        sel_t = np.repeat(toks, N).astype(np.int32)
+        sel_n = np.tile(np.arange(N), len(toks)).astype(np.int32)
+        oracle.mla_decode(w.q, kv_o, c.layout, c.page_size, w.block_table, w.seqlens, c.sq, c.sm_scale, sink=w.sink,
+                          indices=w.indices, causal=c.causal, select=(sel_t, sel_n))
+        dt = time.perf_counter() - t0
+        cpu = {"value": len(toks) / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{len(toks)} query tokens x {N} heads of the {args.config} batch (+ its kv_write), "
+                         f"fp64 C oracle, OpenMP over tokens, {dt:.1f} s"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w, args),
+            "kv_gbps": world * cost["kv_bytes"] / (ms_per_step * 1e-3) / 1e9,
+            "kernel_ms": {"kv_write": statistics.mean(kvw_ms), "decode": statistics.mean(dec_ms),
+                          "combine": statistics.mean(cmb_ms)},
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                    "steps": args.e2e_steps, "includes": "host plan, pinned H2D of q/new rows/slots/block_table/"
+                                                         "seqlens/plan, kv_write, decode, combine, D2H of out+lse"},
+            "gpu_launches": launches_per_step * args.steps,
+            "plan": {"partitions": plan.num_partitions, "groups": plan.groups, "total_splits": plan.total_splits},
+            "clocks": clocks}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -72,6 +72,7 @@ typedef enum {
 #define MLA_BLOCK_ROWS 64       /* KV rows per tile (planner block) */
 #define MLA_GROUP_ROWS 64       /* query rows (token x head) per CTA work item */
 #define MLA_WORKSPACE_HEADER 256
+#define MLA_DECODE_SKIP_COMBINE 1u  /* mla_decode flag: leave split partials in the workspace */
 
 typedef struct {
   int32_t num_partitions;   /* rows of sched produced */
@@ -145,16 +146,19 @@ int mla_decode_plan(const int32_t* cache_seqlens, int32_t batch, int32_t q_token
  *               (mla_workspace_init) before first use.
  *  out          device bf16 [T, num_heads, 512]; lse device float [T, num_heads]
  *               (natural log; -inf and out = 0 for an empty candidate set).
- * num_heads must be 16, 32, 48 or a multiple of 64; q_tokens_per_req*num_heads
- * <= 4096. Requests split by the plan are merged by mla_combine on the same
- * stream inside this call.
+ * num_heads >= 1 and q_tokens_per_req*num_heads <= 4096. Requests split by the
+ * plan are merged by mla_combine on the same stream inside this call unless
+ * flags has MLA_DECODE_SKIP_COMBINE, in which case the caller runs mla_combine
+ * on the workspace partials (layout: MLA_WORKSPACE_HEADER bytes of status, then
+ * part_lse float [total_splits, R] padded to a multiple of 256 bytes, then
+ * part_out float [total_splits, R, 512], R = q_tokens_per_req * num_heads).
  */
 int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
                const int32_t* block_table, int32_t max_pages, const int32_t* cache_seqlens, int32_t batch,
                int32_t q_tokens_per_req, int32_t num_heads, float sm_scale, const float* sink,
                const int32_t* indices, int32_t topk, int32_t causal, const int32_t* sched,
                const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
-               size_t workspace_bytes, void* out, float* lse, void* stream);
+               size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream);
 
 /*
  * Split combine (device): for every request whose split count

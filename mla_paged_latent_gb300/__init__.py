@@ -66,7 +66,7 @@ def load(path: str | None = None):
         lib.mla_page_bytes.argtypes = [I32, I32, ctypes.POINTER(I64)]
         lib.mla_decode_plan.argtypes = [V, I32, I32, I32, I32, I32, I32, V, I32, V, ctypes.POINTER(_PlanInfo)]
         lib.mla_decode.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32, V, V, I32, I32,
-                                   V, SZ, V, V, V]
+                                   V, SZ, V, V, ctypes.c_uint32, V]
         lib.mla_combine.argtypes = [V, V, V, I32, I32, I32, V, V, V, V]
         lib.mla_kv_write.argtypes = [V, V, I32, V, I32, I64, I32, V]
         lib.mla_kv_gather.argtypes = [V, I32, I64, I32, V, I32, I32, V, V]
@@ -142,7 +142,7 @@ def mla_decode_plan(cache_seqlens, q_tokens_per_req: int, num_heads: int, topk: 
 
 def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens, q_tokens_per_req: int,
                sm_scale: float, sched, num_splits, num_partitions: int, total_splits: int, workspace, out, lse,
-               sink=None, indices=None, causal: bool = False, stream=None):
+               sink=None, indices=None, causal: bool = False, skip_combine: bool = False, stream=None):
     """Enqueue decode (+ split combine) on `stream`. All tensors on the GPU:
     q bf16 [T, N, Dqk]; kv_cache uint8 [num_pages, page_bytes]; block_table int32 [B, max_pages];
     cache_seqlens int32 [B]; sched int32 [P, 8]; num_splits int32 [B+1]; workspace uint8;
@@ -155,7 +155,18 @@ def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seql
                              block_table.shape[1], _ptr(cache_seqlens), B, q_tokens_per_req, N, float(sm_scale),
                              _ptr(sink), _ptr(indices), topk, int(bool(causal)), _ptr(sched), _ptr(num_splits),
                              num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
-                             _stream(stream)))
+                             1 if skip_combine else 0, _stream(stream)))
+
+
+def workspace_partials(workspace, total_splits: int, rows_per_req: int):
+    """(part_out [S, R, 512], part_lse [S, R]) float32 views into a decode workspace."""
+    import torch
+    n = total_splits * rows_per_req
+    lse_off = WORKSPACE_HEADER
+    out_off = WORKSPACE_HEADER + ((n * 4 + 255) // 256) * 256
+    part_lse = workspace[lse_off:lse_off + n * 4].view(torch.float32).view(total_splits, rows_per_req)
+    part_out = workspace[out_off:out_off + n * 512 * 4].view(torch.float32).view(total_splits, rows_per_req, 512)
+    return part_out, part_lse
 
 
 def mla_combine(part_out, part_lse, num_splits, rows_per_req: int, num_heads: int, out, lse, sink=None,

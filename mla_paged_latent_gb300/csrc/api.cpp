@@ -144,7 +144,7 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
                int32_t q_tokens_per_req, int32_t num_heads, float sm_scale, const float* sink,
                const int32_t* indices, int32_t topk, int32_t causal, const int32_t* sched,
                const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
-               size_t workspace_bytes, void* out, float* lse, void* stream) {
+               size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream) {
   if (!q || !kv_cache || !block_table || !cache_seqlens || !sched || !num_splits || !workspace || !out || !lse)
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: NULL pointer argument");
   int64_t row_bytes, page_bytes;
@@ -247,7 +247,7 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = mla::launch_decode(v, p, q_map, kv_map, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode: decode launch");
-  if (total_splits > batch) {
+  if (total_splits > batch && !(flags & MLA_DECODE_SKIP_COMBINE)) {
     e = mla::launch_combine(p.part_out, p.part_lse, num_splits, batch, static_cast<int>(R), num_heads, sink, p.out,
                             lse, s);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode: combine launch");

@@ -75,7 +75,12 @@ struct Cfg {
   // the row has 9 slabs (V only needs slabs 0-7); otherwise in two extra slabs.
   static constexpr bool kPInStage = (kNslab == 9);
   static constexpr uint32_t kOffP = kQBytes + 2 * kStageBytes;
-  static constexpr uint32_t kOffMisc = kOffP + (kPInStage ? 0 : 2 * kSlab);
+  // fp8 rows carry group scales up to 2^k, so P is passed to the PV MMA as a bf16
+  // pair P = P_hi + P_lo (P_lo = bf16(P - P_hi)): one extra 8 KB buffer, shared by
+  // both stages (its writer waits for the previous PV to finish).
+  static constexpr bool kPSplit = (LAYOUT != 0);
+  static constexpr uint32_t kOffPLo = kOffP + (kPInStage ? 0 : 2 * kSlab);
+  static constexpr uint32_t kOffMisc = kOffPLo + (kPSplit ? kSlab : 0);
   static constexpr uint32_t kSmem = kOffMisc + sizeof(Misc) + 1024;
   static constexpr int kChunks = (LAYOUT == 0) ? 72 : (kNope / 16 + 8);  // 16-B chunks per stored row
   static constexpr int kChunksPerThread = kChunks / 4;
@@ -249,6 +254,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 const uint64_t b = sdesc_sw128(pa + kk * 32, 16, 1024);
                 mma_bf16_ss(tmem_o + blk * 64, a, b, idesc_o, (first && kk == 0) ? 0u : 1u);
               }
+              if (C::kPSplit) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t a = sdesc_sw128(vs + 2 * blk * kSlab + kk * 2048, kSlab, 1024);
+                  const uint64_t b = sdesc_sw128(sb + C::kOffPLo + kk * 32, 16, 1024);
+                  mma_bf16_ss(tmem_o + blk * 64, a, b, idesc_o, 1u);
+                }
+              }
             }
             mma_commit(bar(kKvEmpty + st));
             mma_commit(bar(kPvDone));
@@ -356,12 +369,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const float alpha = fast_exp2(m_run - m_use);
             float psum = 0.f;
             uint32_t pk[32];
+            uint32_t pl[C::kPSplit ? 32 : 1];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               const float p0 = fast_exp2(s[2 * c] - m_use);
               const float p1 = fast_exp2(s[2 * c + 1] - m_use);
               psum += p0 + p1;
               pk[c] = f32x2_to_bf16x2(p0, p1);
+              if (C::kPSplit) {
+                const float h0 = __uint_as_float(pk[c] << 16), h1 = __uint_as_float(pk[c] & 0xFFFF0000u);
+                pl[c] = f32x2_to_bf16x2(p0 - h0, p1 - h1);
+              }
             }
             l_run = l_run * alpha + psum;
             m_run = m_new;
@@ -373,6 +391,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int c8 = 0; c8 < 8; ++c8)
               st_shared_v4(pa + ((c8 ^ (row & 7)) << 4),
                            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]));
+            if (C::kPSplit) {
+              // the shared P_lo buffer is free once the previous tile's PV has completed
+              if (itj >= 1 && !mbar_wait(bar(kPvDone), (itj - 1) & 1, abort_flag, P.status)) return;
+              const uint32_t pla = sb + C::kOffPLo + row * 128;
+#pragma unroll
+              for (int c8 = 0; c8 < 8; ++c8)
+                st_shared_v4(pla + ((c8 ^ (row & 7)) << 4),
+                             make_uint4(pl[4 * c8], pl[4 * c8 + 1], pl[4 * c8 + 2], pl[4 * c8 + 3]));
+            }
           }
           if (TMA_KV && !sparse) {
             // rows past L in this tile may hold stale or non-finite bytes: zero their V part

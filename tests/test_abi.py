@@ -110,7 +110,7 @@ def _decode_rc(lib, **over):
     return lib.mla_decode(args["q"], args["kv"], args["layout"], args["num_pages"], args["page_size"], args["bt"],
                           args["max_pages"], args["sl"], args["batch"], args["sq"], args["heads"], args["scale"],
                           args["sink"], args["idx"], args["topk"], args["causal"], args["sched"], args["ns"],
-                          args["parts"], args["splits"], args["ws"], args["wsb"], args["out"], args["lse"], None)
+                          args["parts"], args["splits"], args["ws"], args["wsb"], args["out"], args["lse"], 0, None)
 
 
 def test_decode_argument_validation(lib):
