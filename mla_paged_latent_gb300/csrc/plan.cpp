@@ -34,7 +34,8 @@ PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int t
     total += nb[b] + kFixedCost;
     min_nb = std::min(min_nb, nb[b]);
   }
-  int64_t payload = std::max<int64_t>(cdiv(total, parts), kFixedCost + 1);
+  // the 2 * kFixedCost slack keeps the number of partitions <= parts
+  int64_t payload = std::max<int64_t>(cdiv(total, parts) + 2 * kFixedCost, kFixedCost + 1);
   if (min_splits > 1 && batch > 0) {
     const int64_t cap = std::max(1, min_nb / min_splits);
     payload = std::min<int64_t>(payload, cap + kFixedCost);

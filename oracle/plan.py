@@ -16,7 +16,10 @@ Rule
   K_b = topk for sparse decode and cache_seqlens[b] otherwise. An empty request
   keeps one (fully masked) block so that some CTA writes its zero output.
 * Cost of a request = nb_b + FIXED (FIXED = 2 block-equivalents of per-split
-  overhead). payload = max(ceil(sum cost / P), FIXED + 1). With min_splits > 1
+  overhead). payload = max(ceil(sum cost / P) + 2*FIXED, FIXED + 1); the 2*FIXED
+  slack guarantees that the greedy fill below never opens more than P
+  partitions: every closed partition is charged at least payload - FIXED, each
+  continuation adds FIXED, so (P'-1)(payload - 2*FIXED) < sum cost. With min_splits > 1
   the payload is capped at max(1, min_b nb_b // min_splits) + FIXED so that
   every request with at least min_splits blocks is cut into >= min_splits splits.
 * Partitions are filled greedily in request order: each segment taken costs its
@@ -49,7 +52,7 @@ def plan_split_kv(cache_seqlens, sq: int, nheads: int, topk: int, min_splits: in
     P = max(1, num_sms // G)
     nb = [max(1, _cdiv(topk if topk > 0 else L, block_rows)) for L in seqlens]
     total = sum(n + FIXED_COST for n in nb)
-    payload = max(_cdiv(total, P), FIXED_COST + 1)
+    payload = max(_cdiv(total, P) + 2 * FIXED_COST, FIXED_COST + 1)
     if min_splits > 1 and B > 0:
         cap = max(1, min(nb) // min_splits)
         payload = min(payload, cap + FIXED_COST)
