@@ -162,6 +162,34 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
                size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream);
 
 /*
+ * No-allocation decode (device). The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory — a host that
+ * gives its whole GPU memory budget to its own pool and forbids extensions to
+ * call cudaMalloc, a latency-critical loop that must not pay for an allocation
+ * (cudaMalloc may synchronise the device), or a language binding with no way to
+ * allocate CUDA memory. It does exactly what mla_decode does (same arguments,
+ * same results) but uses a workspace the library keeps in a static device array
+ * of MLA_STATIC_WORKSPACE_BYTES, held on every GPU that loads the library until
+ * the process exits. Plans needing more (info.workspace_bytes larger than that)
+ * are rejected with MLA_ERR_WORKSPACE_TOO_SMALL. It allocates nothing.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the one array: calls that overlap on the GPU (several
+ *    streams or host threads) race with each other.
+ *  - Each call clears the status word first. status_out, if not NULL, is a
+ *    device uint32 that receives this call's MLA_STATUS_* bits (stream-ordered).
+ */
+#define MLA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+int mla_decode_static_workspace(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages,
+                                int32_t page_size, const int32_t* block_table, int32_t max_pages,
+                                const int32_t* cache_seqlens, int32_t batch, int32_t q_tokens_per_req,
+                                int32_t num_heads, float sm_scale, const float* sink, const int32_t* indices,
+                                int32_t topk, int32_t causal, const int32_t* sched, const int32_t* num_splits,
+                                int32_t num_partitions, int32_t total_splits, void* out, float* lse,
+                                uint32_t* status_out, void* stream);
+
+/*
  * Split combine (device): for every request whose split count
  * (num_splits[b+1] - num_splits[b]) is at least 2, merge its partials by
  * log-sum-exp — lse = ln sum_s e^(lse_s), out = sum_s e^(lse_s - lse) o_s, a

@@ -48,8 +48,9 @@ class _PlanInfo(ctypes.Structure):
                 ("max_splits", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
 
 
-EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_combine", "mla_kv_write", "mla_kv_gather",
-           "mla_workspace_init", "mla_read_status", "mla_last_error"]
+EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_decode_static_workspace", "mla_combine",
+           "mla_kv_write", "mla_kv_gather", "mla_workspace_init", "mla_read_status", "mla_last_error"]
+STATIC_WORKSPACE_BYTES = 64 << 20
 
 
 def load(path: str | None = None):
@@ -67,6 +68,8 @@ def load(path: str | None = None):
         lib.mla_decode_plan.argtypes = [V, I32, I32, I32, I32, I32, I32, V, I32, V, ctypes.POINTER(_PlanInfo)]
         lib.mla_decode.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32, V, V, I32, I32,
                                    V, SZ, V, V, ctypes.c_uint32, V]
+        lib.mla_decode_static_workspace.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32,
+                                                    V, V, I32, I32, V, V, V, V]
         lib.mla_combine.argtypes = [V, V, V, I32, I32, I32, V, V, V, V]
         lib.mla_kv_write.argtypes = [V, V, I32, V, I32, I64, I32, V]
         lib.mla_kv_gather.argtypes = [V, I32, I64, I32, V, I32, I32, V, V]
@@ -156,6 +159,24 @@ def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seql
                              _ptr(sink), _ptr(indices), topk, int(bool(causal)), _ptr(sched), _ptr(num_splits),
                              num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
                              1 if skip_combine else 0, _stream(stream)))
+
+
+def mla_decode_static_workspace(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens,
+                                q_tokens_per_req: int, sm_scale: float, sched, num_splits, num_partitions: int,
+                                total_splits: int, out, lse, sink=None, indices=None, causal: bool = False,
+                                status_out=None, stream=None):
+    """mla_decode without a caller workspace: for callers that cannot allocate device
+    memory, the library's static device workspace (STATIC_WORKSPACE_BYTES) is used.
+    status_out: optional device int32/uint32 [1] receiving the call's status bits."""
+    _require_cuda(q, kv_cache, block_table, cache_seqlens, sched, num_splits, out, lse, sink, indices, status_out)
+    T, N, D = q.shape
+    B = cache_seqlens.shape[0]
+    topk = 0 if indices is None else int(indices.shape[-1])
+    _check(load().mla_decode_static_workspace(
+        _ptr(q), _ptr(kv_cache), layout, kv_cache.shape[0], page_size, _ptr(block_table), block_table.shape[1],
+        _ptr(cache_seqlens), B, q_tokens_per_req, N, float(sm_scale), _ptr(sink), _ptr(indices), topk,
+        int(bool(causal)), _ptr(sched), _ptr(num_splits), num_partitions, total_splits, _ptr(out), _ptr(lse),
+        _ptr(status_out), _stream(stream)))
 
 
 def workspace_partials(workspace, total_splits: int, rows_per_req: int):

@@ -99,6 +99,14 @@ int current_sm_count(int* n) {
 
 }  // namespace
 
+namespace mla {
+// Lets other translation units of the library report a failure through mla_last_error().
+int set_last_error(int code, const char* msg) {
+  g_last_error = msg;
+  return code;
+}
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_last_error(void) { return g_last_error.c_str(); }
