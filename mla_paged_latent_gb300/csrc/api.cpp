@@ -217,6 +217,7 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
   const size_t nrows = static_cast<size_t>(total_splits) * static_cast<size_t>(R);
   mla::DecodeParams p;
   std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv_cache);
   p.block_table = block_table;
   p.seqlens = cache_seqlens;

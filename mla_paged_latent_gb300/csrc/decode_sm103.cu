@@ -38,26 +38,31 @@ namespace mla {
 namespace {
 
 constexpr uint32_t kSlab = 8192;  // 64 rows x 128 B (64 bf16), SW128
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 40;
 enum Bar {
   kQFull = 0,
   kQEmpty = 1,
-  kKvFull = 2,    // +stage
-  kKvEmpty = 4,   // +stage
-  kSFull = 6,     // +buffer
-  kSFree = 8,     // +buffer
-  kPFull = 10,    // +stage
-  kPvDone = 12,
-  kOFull = 13,
-  kOFree = 14,
-  kFinal = 15
+  kKvFull = 2,    // + stage * 9 + slab: one per 64-dim slab (TMA path); [stage][0] for the converter path
+  kKvEmpty = 20,  // + stage * 5 + k: V slabs 2k, 2k+1 free (k < 4); k = 4: the whole stage free
+  kSFull = 30,    // +buffer
+  kSFree = 32,    // +buffer
+  kPFull = 34,    // +stage
+  kPvDone = 36,
+  kOFull = 37,
+  kOFree = 38,
+  kFinal = 39
 };
+__device__ __forceinline__ int kv_full(int st, int slab) { return kKvFull + st * 9 + slab; }
+__device__ __forceinline__ int kv_empty(int st, int k) { return kKvEmpty + st * 5 + k; }
+// Bytes of KV data the prefetch warp keeps in flight ahead of the stage fills.
+constexpr uint32_t kPrefetchBytes = 320u * 1024u;
 
 struct Misc {
   uint64_t bar[kNumBars];
   uint32_t tmem_base;
   int abort;
-  int pad0, pad1;
+  int progress;  // tiles whose stage fill has been issued (throttles the L2 prefetch warp)
+  int pad0;
   float alpha[2][64];  // per-stage so tile j+1 cannot overwrite what tile j's rescale still reads
   float inv[64];
   float lse2[64];
@@ -138,8 +143,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kKvFull + s), TMA_KV ? 1 : 256);
-      mbar_init(bar(kKvEmpty + s), 1);
+      for (int k = 0; k < 9; ++k) mbar_init(bar(kv_full(s, k)), TMA_KV ? 1 : 256);
+      for (int k = 0; k < 5; ++k) mbar_init(bar(kv_empty(s, k)), 1);
       mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kSFree + s), 64);
       mbar_init(bar(kPFull + s), 128);
@@ -149,6 +154,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(bar(kOFree), 128);
     mbar_init(bar(kFinal), 1);
     misc->abort = 0;
+    misc->progress = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -190,7 +196,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const int L = P.seqlens[r];
           for (int j = lo; j < hi; ++j, ++it) {
             const int st = it & 1;
-            if (it >= 2 && !mbar_wait(bar(kKvEmpty + st), ((it >> 1) - 1) & 1, abort_flag, P.status)) return;
             int pages[8];  // page_size >= 8, so at most 64 / 8 boxes
             uint32_t bytes = 0;
             for (int k = 0; k < nbox; ++k) {
@@ -205,24 +210,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 }
               }
               pages[k] = page;
-              if (page >= 0) bytes += NS * box_rows * 128;
+              if (page >= 0) bytes += box_rows * 128;
             }
-            mbar_arrive_expect_tx(bar(kKvFull + st), bytes);
             const uint32_t dst = C::stage(sb, st);
-            for (int k = 0; k < nbox; ++k) {
-              if (pages[k] < 0) continue;
-              const int in_page = (j * kBlockRows + k * box_rows) & (P.page_size - 1);
-              for (int s = 0; s < NS; ++s)
+            // slab by slab, each as soon as the PV that last read it has finished
+            for (int s = 0; s < NS; ++s) {
+              if (it >= 2 && (s == 8 || (s & 1) == 0) &&
+                  !mbar_wait(bar(kv_empty(st, s == 8 ? 4 : s >> 1)), ((it >> 1) - 1) & 1, abort_flag, P.status))
+                return;
+              mbar_arrive_expect_tx(bar(kv_full(st, s)), bytes);
+              for (int k = 0; k < nbox; ++k) {
+                if (pages[k] < 0) continue;
+                const int in_page = (j * kBlockRows + k * box_rows) & (P.page_size - 1);
                 tma_load_3d(dst + s * kSlab + k * box_rows * 128, &kv_map, s * 64, in_page, pages[k],
-                            bar(kKvFull + st));
+                            bar(kv_full(st, s)));
+              }
             }
+            *reinterpret_cast<volatile int*>(&misc->progress) = it + 1;
           }
         });
       }
       // drain: wait for copies that may still be in flight after an abort
       if (*abort_flag) {
         if (u > 0) mbar_wait_drain(bar(kQFull), (u - 1) & 1);
-        for (int k = 1; k <= 2 && it - k >= 0; ++k) mbar_wait_drain(bar(kKvFull + ((it - k) & 1)), ((it - k) >> 1) & 1);
+        if (TMA_KV)
+          for (int k = 1; k <= 2 && it - k >= 0; ++k)
+            for (int s = 0; s < NS; ++s) mbar_wait_drain(bar(kv_full((it - k) & 1, s)), ((it - k) >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -262,8 +275,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                   mma_bf16_ss(tmem_o + blk * 64, a, b, idesc_o, 1u);
                 }
               }
+              mma_commit(bar(kv_empty(st, blk)));  // V slabs 2blk, 2blk+1 may be refilled
             }
-            mma_commit(bar(kKvEmpty + st));
+            mma_commit(bar(kv_empty(st, 4)));
             mma_commit(bar(kPvDone));
             return true;
           };
@@ -271,13 +285,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           for (int jj = 0; jj < ntile; ++jj) {
             const int itj = it + jj;
             const int st = itj & 1;
-            if (!mbar_wait(bar(kKvFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+            if (!TMA_KV && !mbar_wait(bar(kv_full(st, 0)), (itj >> 1) & 1, abort_flag, P.status)) return;
             if (itj >= 2 && !mbar_wait(bar(kSFree + st), ((itj >> 1) - 1) & 1, abort_flag, P.status)) return;
-            tc_fence_after();
             const uint32_t ks = C::stage(sb, st);
             const uint32_t d = tmem_s + st * 64;
 #pragma unroll 1
             for (int s = 0; s < NS; ++s) {
+              if (TMA_KV && !mbar_wait(bar(kv_full(st, s)), (itj >> 1) & 1, abort_flag, P.status)) return;
+              tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t a = sdesc_sw128(sb + s * kSlab + kk * 32, 16, 1024);
@@ -298,6 +313,74 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       // make sure every MMA issued by this thread has finished before TMEM is freed
       mma_commit(bar(kFinal));
       mbar_wait_drain(bar(kFinal), 0);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ L2 prefetch
+    // Streams the Q rows and KV rows of upcoming tiles from HBM into L2 so that
+    // the stage fills (TMA or converters) find them there. It runs ahead of the
+    // fills by about kPrefetchBytes and never blocks them: a prefetch is a hint.
+    const int64_t tile_bytes = static_cast<int64_t>(kBlockRows) * (P.row_bytes + (LAYOUT != 0 ? 8 : 0));
+    int ahead = static_cast<int>(kPrefetchBytes / tile_bytes);
+    ahead = ahead < 2 ? 2 : ahead;
+    const int box_rows = P.page_size < kBlockRows ? P.page_size : kBlockRows;
+    const int nbox = kBlockRows / box_rows;
+    const int64_t total_rows = static_cast<int64_t>(P.batch) * R;
+    int pit = 0;
+    for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
+      const int part = w / G, g = w % G;
+      for_each_unit(P, part, [&](int r, int lo, int hi, int) {
+        if (*abort_flag) return;
+        if (lane == 0) {
+          const int64_t row0 = static_cast<int64_t>(r) * R + g * kGroupRows;
+          int64_t rows = total_rows - row0;
+          rows = rows > P.qbox_rows ? P.qbox_rows : rows;
+          if (rows > 0) prefetch_l2_bulk(P.q + row0 * (NS * 64), static_cast<uint32_t>(rows * NS * 64 * 2));
+        }
+        const int L = P.seqlens[r];
+        const int tok = r * P.sq + (g * kGroupRows) / P.heads;
+        for (int j = lo; j < hi; ++j, ++pit) {
+          const uint64_t t0 = globaltimer();
+          while (pit >= *reinterpret_cast<volatile int*>(&misc->progress) + ahead) {
+            if (*abort_flag) return;
+            if (globaltimer() - t0 > 20000000ull) break;  // stop throttling after 20 ms
+            __nanosleep(256);
+          }
+          if (sparse) {
+            for (int k = lane; k < kBlockRows; k += 32) {
+              const int kk = j * kBlockRows + k;
+              const int pos = kk < P.topk ? P.indices[static_cast<int64_t>(tok) * P.topk + kk] : -1;
+              if (pos < 0 || pos >= L) continue;
+              const int pi = pos >> P.log2_ps;
+              const int page = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
+              if (page < 0 || page >= P.num_pages) continue;
+              const int off = pos & (P.page_size - 1);
+              const uint8_t* pg = P.kv + static_cast<int64_t>(page) * P.page_bytes;
+              prefetch_l2_bulk(pg + static_cast<int64_t>(off) * P.row_bytes, P.row_bytes);
+              if (LAYOUT != 0) {
+                const uintptr_t sa = reinterpret_cast<uintptr_t>(pg + static_cast<int64_t>(P.page_size) * P.row_bytes +
+                                                                 off * 8);
+                prefetch_l2_bulk(reinterpret_cast<const void*>(sa & ~uintptr_t(15)), 16);
+              }
+            }
+          } else if (lane < nbox) {
+            const int pos0 = j * kBlockRows + lane * box_rows;
+            if (pos0 < L) {
+              const int pi = pos0 >> P.log2_ps;
+              const int page = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
+              if (page >= 0 && page < P.num_pages) {
+                const int rows = (L - pos0) < box_rows ? (L - pos0) : box_rows;
+                const int off = pos0 & (P.page_size - 1);
+                const uint8_t* pg = P.kv + static_cast<int64_t>(page) * P.page_bytes;
+                prefetch_l2_bulk(pg + static_cast<int64_t>(off) * P.row_bytes,
+                                 static_cast<uint32_t>(((rows * P.row_bytes) + 15) & ~15));
+                if (LAYOUT != 0)
+                  prefetch_l2_bulk(pg + static_cast<int64_t>(P.page_size) * P.row_bytes + off * 8,
+                                   static_cast<uint32_t>((rows * 8 + 15) & ~15));
+              }
+            }
+          }
+        }
+      });
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
@@ -332,7 +415,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           bool need = false;
           if (row_thread) {
             if (!mbar_wait(bar(kSFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
-            if (!mbar_wait(bar(kKvFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+            if (!TMA_KV && !mbar_wait(bar(kv_full(st, 0)), (itj >> 1) & 1, abort_flag, P.status)) return;
             tc_fence_after();
             uint32_t sr[64];
             {
@@ -406,7 +489,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             int nvalid = L - j * kBlockRows;
             nvalid = nvalid < 0 ? 0 : nvalid;
             if (nvalid < kBlockRows) {
-              if (!row_thread && !mbar_wait(bar(kKvFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+              for (int s = 0; s < 8; ++s)
+                if (!mbar_wait(bar(kv_full(st, s)), (itj >> 1) & 1, abort_flag, P.status)) return;
               const uint32_t vs = C::stage(sb, st);
               const int nz = (kBlockRows - nvalid) * 8 * 8;  // rows x slabs x 16-B chunks
               for (int idx = wt; idx < nz; idx += 128) {
@@ -505,8 +589,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int tok = r * P.sq + (g * kGroupRows) / P.heads;   // sparse: the group's token
         for (int j = lo; j < hi; ++j, ++it) {
           const int st = it & 1;
-          if (it >= 2 && !mbar_wait(bar(kKvEmpty + st), ((it >> 1) - 1) & 1, abort_flag, P.status)) return;
-          fence_proxy_async_smem();
           int pos;
           bool valid;
           if (sparse) {
@@ -532,12 +614,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
           }
           const unsigned bal = __ballot_sync(0xffffffffu, valid && part4 == 0);
-          if (lane == 0) {
-            uint32_t byte = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) byte |= ((bal >> (4 * k)) & 1u) << k;
-            misc->mask[st][(ct >> 5)] = static_cast<uint8_t>(byte);
-          }
+          // issue this tile's global loads first, then wait for the stage to be free
           constexpr int CPT = C::kChunksPerThread;
           uint4 v[CPT];
 #pragma unroll
@@ -547,6 +624,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           uint2 sc = make_uint2(0, 0);
           if (LAYOUT != 0 && valid) sc = ld_nc_v2(scp);
+          if (it >= 2 && !mbar_wait(bar(kv_empty(st, 4)), ((it >> 1) - 1) & 1, abort_flag, P.status)) return;
+          fence_proxy_async_smem();
+          if (lane == 0) {
+            uint32_t byte = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) byte |= ((bal >> (4 * k)) & 1u) << k;
+            misc->mask[st][(ct >> 5)] = static_cast<uint8_t>(byte);
+          }
           const uint32_t dst = C::stage(sb, st);
 #pragma unroll
           for (int i = 0; i < CPT; ++i) {
@@ -579,7 +664,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
           }
           fence_proxy_async_smem();
-          mbar_arrive(bar(kKvFull + st));
+          mbar_arrive(bar(kv_full(st, 0)));
+          if (ct == 0) *reinterpret_cast<volatile int*>(&misc->progress) = it + 1;
         }
       });
     }

@@ -13,7 +13,8 @@ constexpr int kGroupRows = 64;    // query rows per work item
 constexpr int kDecodeThreads = 512;
 
 struct DecodeParams {
-  const uint8_t* kv;              // paged cache (used by the converter path)
+  const uint16_t* q;              // bf16 [T, heads, dqk] (L2 prefetch; loads use the tensor map)
+  const uint8_t* kv;              // paged cache (converter path and L2 prefetch)
   const int32_t* block_table;     // [batch, max_pages]
   const int32_t* seqlens;         // [batch]
   const float* sink;              // [heads] or null
