@@ -129,7 +129,7 @@ int mla_decode_plan(const int32_t* cache_seqlens, int32_t batch, int32_t q_token
  *  cache_seqlens device int32 [batch]: L_b, context rows including the query
  *               tokens' own new rows (seq_len = context_len + query_len,
  *               "mla_attention.py", MLACommonMetadata).
- *  sm_scale     softmax scale of the scores.
+ *  sm_scale     softmax scale of the scores (positive, finite).
  *  sink         device float [num_heads] per-head sink logit added to the
  *               softmax denominator only, or NULL ("MLA" API page of HALOps,
  *               mla_attention, attn_sink). lse does not include it.

@@ -172,6 +172,8 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
   if (indices != nullptr && q_tokens_per_req > 1 && num_heads % mla::kGroupRows != 0)
     return fail(MLA_ERR_UNSUPPORTED, "mla_decode: sparse decode with several tokens needs heads %% 64 == 0");
   if (total_splits < batch) return fail(MLA_ERR_INVALID_ARG, "mla_decode: total_splits %d < batch %d", total_splits, batch);
+  if (!(sm_scale > 0.f) || !(sm_scale < 1e30f))
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode: sm_scale must be a positive finite number");
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out))
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: q, kv_cache and out must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)

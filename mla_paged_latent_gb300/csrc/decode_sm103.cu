@@ -24,8 +24,9 @@
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: Q once per unit, KV tiles through block_table (bf16 dense)
-//   warp 1      MMA issuer (one thread)
-//   warp 2      TMEM allocator
+//   warp 1      TMEM allocator
+//   warp 2      MMA issuer (one thread)
+//   warp 3      L2 prefetch of upcoming tiles
 //   warps 4-7   softmax (warps 4,5: one query row per thread) + O rescale + epilogue
 //   warps 8-15  converters: fp8 -> bf16 dequantisation and sparse row gathers
 #include <cstdint>
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     misc->progress = 0;
     fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tmem_alloc(smem_addr(&misc->tmem_base), 512);
     tmem_relinquish();
   }
@@ -238,8 +239,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int s = 0; s < NS; ++s) mbar_wait_drain(bar(kv_full((it - k) & 1, s)), ((it - k) >> 1) & 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
+    // (on SMSP 2, away from the softmax warps 4 and 5, whose large unrolled code
+    // would otherwise evict the issue loop from the per-SMSP instruction cache)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
       int it = 0, u = 0;
@@ -252,59 +255,98 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         for_each_unit(P, part, [&](int r, int lo, int hi, int) {
           if (*abort_flag) return;
           const int ntile = hi - lo;
-          auto issue_pv = [&](int itp, bool first) -> bool {
+          // descriptors: constant high bits, the smem address (>> 4) in the low 14 bits;
+          // every operand offset below is added to a precomputed base
+          const uint64_t kmaj = sdesc_sw128(0, 16, 1024);       // K-major: Q, K tile, P^T
+          const uint64_t vmaj = sdesc_sw128(0, kSlab, 1024);    // MN-major: V^T (slab pairs)
+          // PV(j) is issued as soon as P(j) is ready -- in the middle of S(j+1) if need be --
+          // so that the stage it frees is refilled as early as possible.
+          int pend = -1;            // tile whose PV has not been issued yet
+          bool pend_first = false;  // ... and whether it is the unit's first tile
+          auto issue_pv_now = [&](int itp, bool first) {
             const int st = itp & 1;
-            if (!mbar_wait(bar(kPFull + st), (itp >> 1) & 1, abort_flag, P.status)) return false;
-            if (first && u > 0 && !mbar_wait(bar(kOFree), (u - 1) & 1, abort_flag, P.status)) return false;
             tc_fence_after();
-            const uint32_t vs = C::stage(sb, st);
-            const uint32_t pa = C::parea(sb, st);
-#pragma unroll
+            const uint64_t va = vmaj | (C::stage(sb, st) >> 4);
+            const uint64_t pb = kmaj | (C::parea(sb, st) >> 4);
+            const uint64_t plo = kmaj | ((sb + C::kOffPLo) >> 4);
+            // compact (rolled) issue loops: the issuing thread must not stall on instruction fetch
+            uint64_t vblk = va;
+#pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
+              const uint32_t dcol = tmem_o + blk * 64;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = sdesc_sw128(vs + 2 * blk * kSlab + kk * 2048, kSlab, 1024);
-                const uint64_t b = sdesc_sw128(pa + kk * 32, 16, 1024);
-                mma_bf16_ss(tmem_o + blk * 64, a, b, idesc_o, (first && kk == 0) ? 0u : 1u);
-              }
+              for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(dcol, vblk + kk * (2048 >> 4), pb + kk * 2, idesc_o, (first && kk == 0) ? 0u : 1u);
               if (C::kPSplit) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t a = sdesc_sw128(vs + 2 * blk * kSlab + kk * 2048, kSlab, 1024);
-                  const uint64_t b = sdesc_sw128(sb + C::kOffPLo + kk * 32, 16, 1024);
-                  mma_bf16_ss(tmem_o + blk * 64, a, b, idesc_o, 1u);
-                }
+                for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dcol, vblk + kk * (2048 >> 4), plo + kk * 2, idesc_o, 1u);
               }
               mma_commit(bar(kv_empty(st, blk)));  // V slabs 2blk, 2blk+1 may be refilled
+              vblk += (2 * kSlab) >> 4;
             }
             mma_commit(bar(kv_empty(st, 4)));
             mma_commit(bar(kPvDone));
+          };
+          auto pv_ready = [&]() -> bool {
+            return mbar_test_wait(bar(kPFull + (pend & 1)), (pend >> 1) & 1) &&
+                   (!pend_first || u == 0 || mbar_test_wait(bar(kOFree), (u - 1) & 1));
+          };
+          auto try_pv = [&]() {
+            if (pend >= 0 && pv_ready()) {
+              issue_pv_now(pend, pend_first);
+              pend = -1;
+            }
+          };
+          // wait for a phase while issuing the pending PV as soon as it becomes ready
+          auto wait_pv = [&](uint32_t b, uint32_t parity) -> bool {
+            if (mbar_test_wait(b, parity)) return true;
+            const uint64_t t0 = globaltimer();
+            while (true) {
+              try_pv();
+              if (mbar_test_wait(b, parity)) return true;
+              if (*abort_flag) return false;
+              if (globaltimer() - t0 > 2000000000ull) {
+                atomicOr(P.status, 1u);
+                *abort_flag = 1;
+                return false;
+              }
+            }
+          };
+          auto flush_pv = [&]() -> bool {
+            if (pend < 0) return true;
+            if (!mbar_wait(bar(kPFull + (pend & 1)), (pend >> 1) & 1, abort_flag, P.status)) return false;
+            if (pend_first && u > 0 && !mbar_wait(bar(kOFree), (u - 1) & 1, abort_flag, P.status)) return false;
+            issue_pv_now(pend, pend_first);
+            pend = -1;
             return true;
           };
           if (!mbar_wait(bar(kQFull), u & 1, abort_flag, P.status)) return;
+          const uint64_t qa = kmaj | (sb >> 4);
           for (int jj = 0; jj < ntile; ++jj) {
             const int itj = it + jj;
             const int st = itj & 1;
-            if (!TMA_KV && !mbar_wait(bar(kv_full(st, 0)), (itj >> 1) & 1, abort_flag, P.status)) return;
-            if (itj >= 2 && !mbar_wait(bar(kSFree + st), ((itj >> 1) - 1) & 1, abort_flag, P.status)) return;
-            const uint32_t ks = C::stage(sb, st);
+            const uint32_t par = (itj >> 1) & 1;
+            if (!TMA_KV && !wait_pv(bar(kv_full(st, 0)), par)) return;
+            if (itj >= 2 && !wait_pv(bar(kSFree + st), par ^ 1u)) return;
+            tc_fence_after();
+            const uint64_t kb = kmaj | (C::stage(sb, st) >> 4);
             const uint32_t d = tmem_s + st * 64;
+            uint64_t qs = qa, ksd = kb;
 #pragma unroll 1
             for (int s = 0; s < NS; ++s) {
-              if (TMA_KV && !mbar_wait(bar(kv_full(st, s)), (itj >> 1) & 1, abort_flag, P.status)) return;
-              tc_fence_after();
+              if (TMA_KV && !wait_pv(bar(kv_full(st, s)), par)) return;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = sdesc_sw128(sb + s * kSlab + kk * 32, 16, 1024);
-                const uint64_t b = sdesc_sw128(ks + s * kSlab + kk * 32, 16, 1024);
-                mma_bf16_ss(d, a, b, idesc_s, (s | kk) ? 1u : 0u);
-              }
+              for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qs + kk * 2, ksd + kk * 2, idesc_s, (s | kk) ? 1u : 0u);
+              qs += kSlab >> 4;
+              ksd += kSlab >> 4;
             }
             mma_commit(bar(kSFull + st));
             if (jj == ntile - 1) mma_commit(bar(kQEmpty));
-            if (jj >= 1 && !issue_pv(itj - 1, jj == 1)) return;
+            if (!flush_pv()) return;  // at most one PV outstanding
+            pend = itj;
+            pend_first = (jj == 0);
           }
-          if (!issue_pv(it + ntile - 1, ntile == 1)) return;
+          if (!flush_pv()) return;
           mma_commit(bar(kOFull));
           it += ntile;
           ++u;
@@ -414,61 +456,59 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const bool first = jj == 0;
           bool need = false;
           if (row_thread) {
-            if (!mbar_wait(bar(kSFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
-            if (!TMA_KV && !mbar_wait(bar(kv_full(st, 0)), (itj >> 1) & 1, abort_flag, P.status)) return;
+            const uint32_t par = (itj >> 1) & 1;
+            if (!mbar_wait(bar(kSFull + st), par, abort_flag, P.status)) return;
+            if (!TMA_KV && !mbar_wait(bar(kv_full(st, 0)), par, abort_flag, P.status)) return;
             tc_fence_after();
             uint32_t sr[64];
-            {
-              uint32_t t16[16];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                tmem_ld16(tmem_s + st * 64 + lane_off + c * 16, t16);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sr[c * 16 + i] = t16[i];
-              }
-            }
+            tmem_ld32(tmem_s + st * 64 + lane_off, sr);
+            tmem_ld32(tmem_s + st * 64 + lane_off + 32, sr + 32);
+            tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(kSFree + st));
-            float s[64];
-            uint64_t vmask = 0;
+            // mask (raw scores; the positive scale is folded into the exponent below)
+            uint64_t vmask;
             if (sparse || !TMA_KV) {
+              vmask = 0;
 #pragma unroll
               for (int k = 0; k < 8; ++k) vmask |= static_cast<uint64_t>(misc->mask[st][k]) << (8 * k);
             }
-            float mt = -INFINITY;
+            if (!sparse) {
+              int nv = lim - j * kBlockRows;
+              nv = nv < 0 ? 0 : (nv > 64 ? 64 : nv);
+              vmask = nv == 64 ? ~0ull : ((1ull << nv) - 1ull);
+            }
+            if (!valid_row) vmask = 0;
+            float x[64];
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-              bool ok;
-              if (sparse) ok = (vmask >> c) & 1ull;
-              else ok = (j * kBlockRows + c) < lim;
-              ok = ok && valid_row;
-              s[c] = ok ? __uint_as_float(sr[c]) * P.scale_log2 : -INFINITY;
-              mt = fmaxf(mt, s[c]);
+              x[c] = ((vmask >> c) & 1ull) ? __uint_as_float(sr[c]) : -INFINITY;
+              m4[c & 3] = fmaxf(m4[c & 3], x[c]);
             }
+            const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
             const float m_new = (mt > m_run + 8.0f) ? mt : m_run;
             need = (m_new != m_run) && (m_run != -INFINITY) && !first;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = fast_exp2(m_run - m_use);
-            float psum = 0.f;
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[32];
             uint32_t pl[C::kPSplit ? 32 : 1];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              const float p0 = fast_exp2(s[2 * c] - m_use);
-              const float p1 = fast_exp2(s[2 * c + 1] - m_use);
-              psum += p0 + p1;
+              const float p0 = fast_exp2(fmaf(x[2 * c], P.scale_log2, -m_use));
+              const float p1 = fast_exp2(fmaf(x[2 * c + 1], P.scale_log2, -m_use));
+              ps4[c & 3] += p0 + p1;
               pk[c] = f32x2_to_bf16x2(p0, p1);
               if (C::kPSplit) {
                 const float h0 = __uint_as_float(pk[c] << 16), h1 = __uint_as_float(pk[c] & 0xFFFF0000u);
                 pl[c] = f32x2_to_bf16x2(p0 - h0, p1 - h1);
               }
             }
-            l_run = l_run * alpha + psum;
+            l_run = l_run * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
             m_run = m_new;
             misc->alpha[st][row] = need ? alpha : 1.0f;
             // P^T row `row`: 64 bf16 along KV, K-major 128-B swizzled
-            fence_proxy_async_smem();
             const uint32_t pa = C::parea(sb, st) + row * 128;
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
@@ -674,7 +714,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
