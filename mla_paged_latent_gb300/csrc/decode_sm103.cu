@@ -24,8 +24,8 @@
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: Q once per unit, KV tiles through block_table (bf16 dense)
-//   warp 1      TMEM allocator
-//   warp 2      MMA issuer (one thread)
+//   warp 1      TMEM allocator; PV MMA issuer (one thread)
+//   warp 2      S MMA issuer (one thread)
 //   warp 3      L2 prefetch of upcoming tiles
 //   warps 4-7   softmax (warps 4,5: one query row per thread) + O rescale + epilogue
 //   warps 8-15  converters: fp8 -> bf16 dequantisation and sparse row gathers
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(bar(kPvDone), 1);
     mbar_init(bar(kOFull), 1);
     mbar_init(bar(kOFree), 128);
-    mbar_init(bar(kFinal), 1);
+    mbar_init(bar(kFinal), 2);  // one commit from each MMA issuer
     misc->abort = 0;
     misc->progress = 0;
     fence_mbar_init();
@@ -240,11 +240,62 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
     }
   } else if (warp == 2) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     // (on SMSP 2, away from the softmax warps 4 and 5, whose large unrolled code
-    // would otherwise evict the issue loop from the per-SMSP instruction cache)
+    // would otherwise evict the issue loop from the per-SMSP instruction cache).
+    // S and PV are issued by two threads: a thread that polls a barrier stalls
+    // until the MMAs it has queued are dispatched, so a single issuer either
+    // leaves the tensor pipe idle while it checks whether P is ready or issues
+    // PV late. With two issuers, each waits only for its own operands and the
+    // tensor pipe interleaves S(j+1) with PV(j) as soon as P(j) exists, which
+    // frees each stage (and starts its refill) as early as possible.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
+      const uint64_t kmaj = sdesc_sw128(0, 16, 1024);  // K-major: Q, K tile
+      const uint64_t qa = kmaj | (sb >> 4);
+      int it = 0, u = 0;
+      for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
+        const int part = w / G;
+        for_each_unit(P, part, [&](int, int lo, int hi, int) {
+          if (*abort_flag) return;
+          const int ntile = hi - lo;
+          if (!mbar_wait(bar(kQFull), u & 1, abort_flag, P.status)) return;
+          for (int jj = 0; jj < ntile; ++jj) {
+            const int itj = it + jj;
+            const int st = itj & 1;
+            const uint32_t par = (itj >> 1) & 1;
+            if (!TMA_KV && !mbar_wait(bar(kv_full(st, 0)), par, abort_flag, P.status)) return;
+            if (itj >= 2 && !mbar_wait(bar(kSFree + st), par ^ 1u, abort_flag, P.status)) return;
+            tc_fence_after();
+            const uint32_t d = tmem_s + st * 64;
+            uint64_t qs = qa, ksd = kmaj | (C::stage(sb, st) >> 4);
+#pragma unroll 1
+            for (int s = 0; s < NS; ++s) {
+              if (TMA_KV && !mbar_wait(bar(kv_full(st, s)), par, abort_flag, P.status)) return;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qs + kk * 2, ksd + kk * 2, idesc_s, (s | kk) ? 1u : 0u);
+              qs += kSlab >> 4;
+              ksd += kSlab >> 4;
+            }
+            mma_commit(bar(kSFull + st));
+          }
+          mma_commit(bar(kQEmpty));
+          it += ntile;
+          ++u;
+        });
+      }
+      // every MMA this thread issued must finish before TMEM is freed
+      mma_commit(bar(kFinal));
+      mbar_wait_drain(bar(kFinal), 0);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ PV issuer
+    // O^T += V^T P^T for each tile as soon as the softmax has written P^T(j)
+    // (and, for a unit's first tile, the epilogue has read the previous O^T).
+    if (lane == 0) {
+      const uint64_t kmaj = sdesc_sw128(0, 16, 1024);     // K-major: P^T
+      const uint64_t vmaj = sdesc_sw128(0, kSlab, 1024);  // MN-major: V^T (slab pairs)
+      const uint64_t plo = kmaj | ((sb + C::kOffPLo) >> 4);
       int it = 0, u = 0;
       for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
         const int part = w / G, g = w % G;
@@ -252,31 +303,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         rows_g = rows_g > kGroupRows ? kGroupRows : rows_g;
         const int nq = (rows_g + 15) & ~15;
         const uint32_t idesc_o = idesc_bf16_f32(128, nq, 1, 0);
-        for_each_unit(P, part, [&](int r, int lo, int hi, int) {
+        for_each_unit(P, part, [&](int, int lo, int hi, int) {
           if (*abort_flag) return;
           const int ntile = hi - lo;
-          // descriptors: constant high bits, the smem address (>> 4) in the low 14 bits;
-          // every operand offset below is added to a precomputed base
-          const uint64_t kmaj = sdesc_sw128(0, 16, 1024);       // K-major: Q, K tile, P^T
-          const uint64_t vmaj = sdesc_sw128(0, kSlab, 1024);    // MN-major: V^T (slab pairs)
-          // PV(j) is issued as soon as P(j) is ready -- in the middle of S(j+1) if need be --
-          // so that the stage it frees is refilled as early as possible.
-          int pend = -1;            // tile whose PV has not been issued yet
-          bool pend_first = false;  // ... and whether it is the unit's first tile
-          auto issue_pv_now = [&](int itp, bool first) {
-            const int st = itp & 1;
+          for (int jj = 0; jj < ntile; ++jj) {
+            const int itj = it + jj;
+            const int st = itj & 1;
+            if (!mbar_wait(bar(kPFull + st), (itj >> 1) & 1, abort_flag, P.status)) return;
+            if (jj == 0 && u > 0 && !mbar_wait(bar(kOFree), (u - 1) & 1, abort_flag, P.status)) return;
             tc_fence_after();
-            const uint64_t va = vmaj | (C::stage(sb, st) >> 4);
             const uint64_t pb = kmaj | (C::parea(sb, st) >> 4);
-            const uint64_t plo = kmaj | ((sb + C::kOffPLo) >> 4);
-            // compact (rolled) issue loops: the issuing thread must not stall on instruction fetch
-            uint64_t vblk = va;
+            // compact (rolled) issue loop: the issuing thread must not stall on instruction fetch
+            uint64_t vblk = vmaj | (C::stage(sb, st) >> 4);
 #pragma unroll 1
             for (int blk = 0; blk < 4; ++blk) {
               const uint32_t dcol = tmem_o + blk * 64;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(dcol, vblk + kk * (2048 >> 4), pb + kk * 2, idesc_o, (first && kk == 0) ? 0u : 1u);
+                mma_bf16_ss(dcol, vblk + kk * (2048 >> 4), pb + kk * 2, idesc_o, (jj == 0 && kk == 0) ? 0u : 1u);
               if (C::kPSplit) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dcol, vblk + kk * (2048 >> 4), plo + kk * 2, idesc_o, 1u);
@@ -286,73 +330,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
             mma_commit(bar(kv_empty(st, 4)));
             mma_commit(bar(kPvDone));
-          };
-          auto pv_ready = [&]() -> bool {
-            return mbar_test_wait(bar(kPFull + (pend & 1)), (pend >> 1) & 1) &&
-                   (!pend_first || u == 0 || mbar_test_wait(bar(kOFree), (u - 1) & 1));
-          };
-          auto try_pv = [&]() {
-            if (pend >= 0 && pv_ready()) {
-              issue_pv_now(pend, pend_first);
-              pend = -1;
-            }
-          };
-          // wait for a phase while issuing the pending PV as soon as it becomes ready
-          auto wait_pv = [&](uint32_t b, uint32_t parity) -> bool {
-            if (mbar_test_wait(b, parity)) return true;
-            const uint64_t t0 = globaltimer();
-            while (true) {
-              try_pv();
-              if (mbar_test_wait(b, parity)) return true;
-              if (*abort_flag) return false;
-              if (globaltimer() - t0 > 2000000000ull) {
-                atomicOr(P.status, 1u);
-                *abort_flag = 1;
-                return false;
-              }
-            }
-          };
-          auto flush_pv = [&]() -> bool {
-            if (pend < 0) return true;
-            if (!mbar_wait(bar(kPFull + (pend & 1)), (pend >> 1) & 1, abort_flag, P.status)) return false;
-            if (pend_first && u > 0 && !mbar_wait(bar(kOFree), (u - 1) & 1, abort_flag, P.status)) return false;
-            issue_pv_now(pend, pend_first);
-            pend = -1;
-            return true;
-          };
-          if (!mbar_wait(bar(kQFull), u & 1, abort_flag, P.status)) return;
-          const uint64_t qa = kmaj | (sb >> 4);
-          for (int jj = 0; jj < ntile; ++jj) {
-            const int itj = it + jj;
-            const int st = itj & 1;
-            const uint32_t par = (itj >> 1) & 1;
-            if (!TMA_KV && !wait_pv(bar(kv_full(st, 0)), par)) return;
-            if (itj >= 2 && !wait_pv(bar(kSFree + st), par ^ 1u)) return;
-            tc_fence_after();
-            const uint64_t kb = kmaj | (C::stage(sb, st) >> 4);
-            const uint32_t d = tmem_s + st * 64;
-            uint64_t qs = qa, ksd = kb;
-#pragma unroll 1
-            for (int s = 0; s < NS; ++s) {
-              if (TMA_KV && !wait_pv(bar(kv_full(st, s)), par)) return;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qs + kk * 2, ksd + kk * 2, idesc_s, (s | kk) ? 1u : 0u);
-              qs += kSlab >> 4;
-              ksd += kSlab >> 4;
-            }
-            mma_commit(bar(kSFull + st));
-            if (jj == ntile - 1) mma_commit(bar(kQEmpty));
-            if (!flush_pv()) return;  // at most one PV outstanding
-            pend = itj;
-            pend_first = (jj == 0);
           }
-          if (!flush_pv()) return;
           mma_commit(bar(kOFull));
           it += ntile;
           ++u;
         });
       }
-      // make sure every MMA issued by this thread has finished before TMEM is freed
       mma_commit(bar(kFinal));
       mbar_wait_drain(bar(kFinal), 0);
     }
