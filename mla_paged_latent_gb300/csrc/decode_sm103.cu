@@ -32,6 +32,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "decode_common.cuh"
 #include "mla_kernels.h"
 #include "ptx_sm103.cuh"
 
@@ -43,7 +44,7 @@ constexpr int kNumBars = 40;
 enum Bar {
   kQFull = 0,
   kQEmpty = 1,
-  kKvFull = 2,    // + stage * 9 + slab: one per 64-dim slab (TMA path); [stage][0] for the converter path
+  kKvFull = 2,    // + stage * 9 + group: slabs 4g..4g+3 (TMA path); [stage][0] for the converter path
   kKvEmpty = 20,  // + stage * 5 + k: V slabs 2k, 2k+1 free (k < 4); k = 4: the whole stage free
   kSFull = 30,    // +buffer
   kSFree = 32,    // +buffer
@@ -53,7 +54,10 @@ enum Bar {
   kOFree = 38,
   kFinal = 39
 };
-__device__ __forceinline__ int kv_full(int st, int slab) { return kKvFull + st * 9 + slab; }
+__device__ __forceinline__ int kv_full(int st, int grp) { return kKvFull + st * 9 + grp; }
+// TMA path: the S issuer checks one barrier per group of 4 slabs (each check stalls it
+// until its queued MMAs are dispatched, so fewer checks keep the tensor pipe busier).
+__device__ __forceinline__ int slab_group(int s) { return s >> 2; }
 __device__ __forceinline__ int kv_empty(int st, int k) { return kKvEmpty + st * 5 + k; }
 // Bytes of KV data the prefetch warp keeps in flight ahead of the stage fills.
 constexpr uint32_t kPrefetchBytes = 320u * 1024u;
@@ -64,7 +68,7 @@ struct Misc {
   int abort;
   int progress;  // tiles whose stage fill has been issued (throttles the L2 prefetch warp)
   int pad0;
-  float alpha[2][64];  // per-stage so tile j+1 cannot overwrite what tile j's rescale still reads
+  float alpha[2][64];  // per stage: tile j+1 must not overwrite what tile j's rescale reads
   float inv[64];
   float lse2[64];
   uint8_t mask[2][8];  // sparse / gathered row validity per stage, one byte per 8 rows
@@ -96,32 +100,6 @@ struct Cfg {
   }
 };
 
-__device__ __forceinline__ int num_blocks(const DecodeParams& P, int r) {
-  const int K = P.topk > 0 ? P.topk : P.seqlens[r];
-  const int nb = (K + kBlockRows - 1) / kBlockRows;
-  return nb < 1 ? 1 : nb;
-}
-
-// Segments (request, block range, split index) of one partition, in order.
-template <typename F>
-__device__ __forceinline__ void for_each_unit(const DecodeParams& P, int part, F&& f) {
-  const int* s = P.sched + 8 * part;
-  const int b0 = s[0], k0 = s[1], b1 = s[2], k1 = s[3], fs = s[4];
-  for (int r = b0; r < P.batch && (r < b1 || (r == b1 && k1 > 0)); ++r) {
-    const int nb = num_blocks(P, r);
-    const int lo = (r == b0) ? k0 : 0;
-    const int hi = (r == b1) ? (k1 < nb ? k1 : nb) : nb;
-    if (hi <= lo) continue;
-    f(r, lo, hi, (r == b0) ? fs : 0);
-  }
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 template <int LAYOUT, bool TMA_KV>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     mla_decode_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap q_map,
@@ -144,7 +122,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
-      for (int k = 0; k < 9; ++k) mbar_init(bar(kv_full(s, k)), TMA_KV ? 1 : 256);
+      for (int k = 0; k < 9; ++k) {
+        // TMA path: one arrival (with its bytes) per slab of the group
+        const int nslab_g = NS - 4 * k < 4 ? NS - 4 * k : 4;
+        mbar_init(bar(kv_full(s, k)), TMA_KV ? (nslab_g > 0 ? nslab_g : 1) : 256);
+      }
       for (int k = 0; k < 5; ++k) mbar_init(bar(kv_empty(s, k)), 1);
       mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kSFree + s), 64);
@@ -219,12 +201,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               if (it >= 2 && (s == 8 || (s & 1) == 0) &&
                   !mbar_wait(bar(kv_empty(st, s == 8 ? 4 : s >> 1)), ((it >> 1) - 1) & 1, abort_flag, P.status))
                 return;
-              mbar_arrive_expect_tx(bar(kv_full(st, s)), bytes);
+              mbar_arrive_expect_tx(bar(kv_full(st, slab_group(s))), bytes);
               for (int k = 0; k < nbox; ++k) {
                 if (pages[k] < 0) continue;
                 const int in_page = (j * kBlockRows + k * box_rows) & (P.page_size - 1);
                 tma_load_3d(dst + s * kSlab + k * box_rows * 128, &kv_map, s * 64, in_page, pages[k],
-                            bar(kv_full(st, s)));
+                            bar(kv_full(st, slab_group(s))));
               }
             }
             *reinterpret_cast<volatile int*>(&misc->progress) = it + 1;
@@ -236,7 +218,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (u > 0) mbar_wait_drain(bar(kQFull), (u - 1) & 1);
         if (TMA_KV)
           for (int k = 1; k <= 2 && it - k >= 0; ++k)
-            for (int s = 0; s < NS; ++s) mbar_wait_drain(bar(kv_full((it - k) & 1, s)), ((it - k) >> 1) & 1);
+            for (int gq = 0; gq <= slab_group(NS - 1); ++gq)
+              mbar_wait_drain(bar(kv_full((it - k) & 1, gq)), ((it - k) >> 1) & 1);
       }
     }
   } else if (warp == 2) {
@@ -271,7 +254,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             uint64_t qs = qa, ksd = kmaj | (C::stage(sb, st) >> 4);
 #pragma unroll 1
             for (int s = 0; s < NS; ++s) {
-              if (TMA_KV && !mbar_wait(bar(kv_full(st, s)), par, abort_flag, P.status)) return;
+              if (TMA_KV && (s & 3) == 0 && !mbar_wait(bar(kv_full(st, slab_group(s))), par, abort_flag, P.status))
+                return;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(d, qs + kk * 2, ksd + kk * 2, idesc_s, (s | kk) ? 1u : 0u);
               qs += kSlab >> 4;
@@ -409,18 +393,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
+    // Warps 4-7 meet at named barriers (a waiting warp sleeps instead of taking
+    // issue slots from the MMA issuers on the same SM sub-partitions). A named
+    // barrier has no time limit, so these warps never leave one another behind:
+    // a thread whose bounded wait fails only marks itself `dead` and carries on
+    // through the barriers, every barrier ORs the mark in, and all four warps stop
+    // together at the barrier where it becomes visible.
     const int wt = tid - 128;                 // 0..127, TMEM lane of this thread
     const uint32_t lane_off = static_cast<uint32_t>((wt & ~31)) << 16;
     const bool row_thread = wt < 64;
     const int row = wt;
+    bool dead = false, stop = false;
+    auto wait = [&](uint32_t b, uint32_t parity) {
+      if (!dead && !mbar_wait(b, parity, abort_flag, P.status)) dead = true;
+      return !dead;
+    };
     int it = 0, u = 0;
-    for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
+    for (int w = blockIdx.x; w < P.num_work && !stop; w += gridDim.x) {
       const int part = w / G, g = w % G;
       int rows_g = R - g * kGroupRows;
       rows_g = rows_g > kGroupRows ? kGroupRows : rows_g;
       const int nq = (rows_g + 15) & ~15;
       for_each_unit(P, part, [&](int r, int lo, int hi, int sidx) {
-        if (*abort_flag) return;
+        if (stop) return;
         const int L = P.seqlens[r];
         const int grow = g * kGroupRows + row;          // query row within the request
         const bool valid_row = row_thread && row < rows_g;
@@ -440,8 +435,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           bool need = false;
           if (row_thread) {
             const uint32_t par = (itj >> 1) & 1;
-            if (!mbar_wait(bar(kSFull + st), par, abort_flag, P.status)) return;
-            if (!TMA_KV && !mbar_wait(bar(kv_full(st, 0)), par, abort_flag, P.status)) return;
+            wait(bar(kSFull + st), par);
+            if (!TMA_KV) wait(bar(kv_full(st, 0)), par);
+          }
+          if (row_thread && !dead) {
             tc_fence_after();
             uint32_t sr[64];
             tmem_ld32(tmem_s + st * 64 + lane_off, sr);
@@ -497,9 +494,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int c8 = 0; c8 < 8; ++c8)
               st_shared_v4(pa + ((c8 ^ (row & 7)) << 4),
                            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]));
-            if (C::kPSplit) {
-              // the shared P_lo buffer is free once the previous tile's PV has completed
-              if (itj >= 1 && !mbar_wait(bar(kPvDone), (itj - 1) & 1, abort_flag, P.status)) return;
+            // the shared P_lo buffer is free once the previous tile's PV has completed
+            if (C::kPSplit && (itj == 0 || wait(bar(kPvDone), (itj - 1) & 1))) {
               const uint32_t pla = sb + C::kOffPLo + row * 128;
 #pragma unroll
               for (int c8 = 0; c8 < 8; ++c8)
@@ -512,38 +508,45 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             int nvalid = L - j * kBlockRows;
             nvalid = nvalid < 0 ? 0 : nvalid;
             if (nvalid < kBlockRows) {
-              for (int s = 0; s < 8; ++s)
-                if (!mbar_wait(bar(kv_full(st, s)), (itj >> 1) & 1, abort_flag, P.status)) return;
-              const uint32_t vs = C::stage(sb, st);
-              const int nz = (kBlockRows - nvalid) * 8 * 8;  // rows x slabs x 16-B chunks
-              for (int idx = wt; idx < nz; idx += 128) {
-                const int rr = nvalid + idx / 64;
-                const int sl = (idx / 8) & 7;
-                const int ch = idx & 7;
-                st_shared_v4(vs + sl * kSlab + rr * 128 + ch * 16, make_uint4(0, 0, 0, 0));
+              for (int gq = 0; gq < 2; ++gq) wait(bar(kv_full(st, gq)), (itj >> 1) & 1);
+              if (!dead) {
+                const uint32_t vs = C::stage(sb, st);
+                const int nz = (kBlockRows - nvalid) * 8 * 8;  // rows x slabs x 16-B chunks
+                for (int idx = wt; idx < nz; idx += 128) {
+                  const int rr = nvalid + idx / 64;
+                  const int sl = (idx / 8) & 7;
+                  const int ch = idx & 7;
+                  st_shared_v4(vs + sl * kSlab + rr * 128 + ch * 16, make_uint4(0, 0, 0, 0));
+                }
               }
             }
           }
           fence_proxy_async_smem();
-          const bool any_need = named_bar_or(1, 128, need);
-          if (any_need) {
-            if (!mbar_wait(bar(kPvDone), (itj - 1) & 1, abort_flag, P.status)) return;
-            tc_fence_after();
-            for (int blk = 0; blk < 4; ++blk) {
-              for (int c = 0; c < nq; c += 16) {
-                uint32_t t16[16];
-                const uint32_t ta = tmem_o + lane_off + blk * 64 + c;
-                tmem_ld16(ta, t16);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) t16[i] = __float_as_uint(__uint_as_float(t16[i]) * misc->alpha[st][c + i]);
-                tmem_st16(ta, t16);
-              }
+          // rescale needed anywhere, or a thread has given up (then everyone stops here)
+          if (named_bar_or(1, 128, need || dead)) {
+            if (named_bar_or(1, 128, dead)) {
+              stop = true;
+              return;
             }
-            tmem_wait_st();
-            tc_fence_before();
+            if (wait(bar(kPvDone), (itj - 1) & 1)) {
+              tc_fence_after();
+              for (int blk = 0; blk < 4; ++blk) {
+                for (int c = 0; c < nq; c += 16) {
+                  uint32_t t16[16];
+                  const uint32_t ta = tmem_o + lane_off + blk * 64 + c;
+                  tmem_ld16(ta, t16);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    t16[i] = __float_as_uint(__uint_as_float(t16[i]) * misc->alpha[st][c + i]);
+                  tmem_st16(ta, t16);
+                }
+              }
+              tmem_wait_st();
+              tc_fence_before();
+            }
           }
-          mbar_arrive(bar(kPFull + st));
+          if (!dead) mbar_arrive(bar(kPFull + st));
         }
         // -------------------------------------------------------- epilogue
         const int base_split = P.num_splits[r];
@@ -562,42 +565,47 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           misc->inv[row] = inv;
           misc->lse2[row] = lse2;
-          if (valid_row) {
+          if (valid_row && !dead) {
             const float lse_nat = lse2 * 0.6931471805599453f;
             if (nsplit == 1) P.lse[(int64_t)r * R + grow] = lse_nat;
             else P.part_lse[(int64_t)sg * R + grow] = lse_nat;
           }
         }
-        named_bar_sync(1, 128);
-        if (!mbar_wait(bar(kOFull), u & 1, abort_flag, P.status)) return;
-        tc_fence_after();
-        for (int blk = 0; blk < 4; ++blk) {
-          const int d = blk * 128 + wt;
-          for (int c = 0; c < nq; c += 16) {
-            uint32_t t16[16];
-            tmem_ld16(tmem_o + lane_off + blk * 64 + c, t16);
-            tmem_wait_ld();
+        if (named_bar_or(1, 128, dead)) {
+          stop = true;
+          return;
+        }
+        if (wait(bar(kOFull), u & 1)) {
+          tc_fence_after();
+          for (int blk = 0; blk < 4; ++blk) {
+            const int d = blk * 128 + wt;
+            for (int c = 0; c < nq; c += 16) {
+              uint32_t t16[16];
+              tmem_ld16(tmem_o + lane_off + blk * 64 + c, t16);
+              tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int qr = c + i;
-              if (qr >= rows_g) break;
-              const float v = __uint_as_float(t16[i]) * misc->inv[qr];
-              const int64_t flat = (int64_t)r * R + g * kGroupRows + qr;
-              if (nsplit == 1) {
-                const uint32_t b = f32x2_to_bf16x2(v, 0.f);
-                P.out[flat * 512 + d] = static_cast<uint16_t>(b & 0xFFFFu);
-              } else {
-                P.part_out[((int64_t)sg * R + g * kGroupRows + qr) * 512 + d] = v;
+              for (int i = 0; i < 16; ++i) {
+                const int qr = c + i;
+                if (qr >= rows_g) break;
+                const float v = __uint_as_float(t16[i]) * misc->inv[qr];
+                const int64_t flat = (int64_t)r * R + g * kGroupRows + qr;
+                if (nsplit == 1) {
+                  const uint32_t b = f32x2_to_bf16x2(v, 0.f);
+                  P.out[flat * 512 + d] = static_cast<uint16_t>(b & 0xFFFFu);
+                } else {
+                  P.part_out[((int64_t)sg * R + g * kGroupRows + qr) * 512 + d] = v;
+                }
               }
             }
           }
+          tc_fence_before();
+          mbar_arrive(bar(kOFree));
         }
-        tc_fence_before();
-        mbar_arrive(bar(kOFree));
         it += ntile;
         ++u;
       });
     }
+    // a thread that gave up after the last barrier of its last unit: nothing left to share
   } else if (warp >= 8 && !TMA_KV) {
     // ------------------------------------------------------------ converters
     const int ct = tid - 256;        // 0..255
