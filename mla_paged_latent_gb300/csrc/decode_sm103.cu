@@ -15,7 +15,7 @@
 //   S   = Q K^T      tcgen05 MMA, M = 128 (query rows; rows >= 64 unused),
 //                    N = 64 KV rows, K = 576 / 512, fp32 accumulator in TMEM
 //   P   = online softmax of S (exp2 domain, lazy rescale when the running max
-//                    grows by more than 2^8), written as bf16 to shared memory
+//                    grows by more than kRescaleLog2), written as bf16 to shared memory
 //   O^T += V^T P^T   tcgen05 MMA, M = 128 value dims (4 blocks), N = query rows,
 //                    K = 64 KV rows, fp32 accumulator in TMEM (256 columns)
 // The transposed output accumulator keeps O for 64 query rows x 512 dims in
@@ -61,6 +61,12 @@ __device__ __forceinline__ int slab_group(int s) { return s >> 2; }
 __device__ __forceinline__ int kv_empty(int st, int k) { return kKvEmpty + st * 5 + k; }
 // Bytes of KV data the prefetch warp keeps in flight ahead of the stage fills.
 constexpr uint32_t kPrefetchBytes = 320u * 1024u;
+// Lazy rescale: P = 2^(s - m) is taken against the running maximum m, which is
+// raised (and O^T rescaled in TMEM) only when a tile's maximum exceeds it by
+// more than this many powers of two. P then stays below 2^32, far inside bf16
+// and fp32 range (O^T <= rows x 2^32 x max|V|); a small threshold rescales on
+// most tiles when the scores spread widely (fp8 rows with group scales).
+constexpr float kRescaleLog2 = 32.0f;
 
 struct Misc {
   uint64_t bar[kNumBars];
@@ -467,7 +473,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               m4[c & 3] = fmaxf(m4[c & 3], x[c]);
             }
             const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
-            const float m_new = (mt > m_run + 8.0f) ? mt : m_run;
+            const float m_new = (mt > m_run + kRescaleLog2) ? mt : m_run;
             need = (m_new != m_run) && (m_run != -INFINITY) && !first;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = fast_exp2(m_run - m_use);
@@ -530,17 +536,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             }
             if (wait(bar(kPvDone), (itj - 1) & 1)) {
               tc_fence_after();
-              for (int blk = 0; blk < 4; ++blk) {
-                for (int c = 0; c < nq; c += 16) {
-                  uint32_t t16[16];
-                  const uint32_t ta = tmem_o + lane_off + blk * 64 + c;
-                  tmem_ld16(ta, t16);
-                  tmem_wait_ld();
+              // one TMEM round trip per 32 columns (columns past nq hold no query row)
+              const float* al = misc->alpha[st];
+#pragma unroll 1
+              for (int k = 0; k < 8; ++k) {
+                uint32_t t32[32];
+                const uint32_t ta = tmem_o + lane_off + k * 32;
+                tmem_ld32(ta, t32);
+                tmem_wait_ld();
+                const float* ak = al + (k & 1) * 32;
 #pragma unroll
-                  for (int i = 0; i < 16; ++i)
-                    t16[i] = __float_as_uint(__uint_as_float(t16[i]) * misc->alpha[st][c + i]);
-                  tmem_st16(ta, t16);
-                }
+                for (int i = 0; i < 32; ++i) t32[i] = __float_as_uint(__uint_as_float(t32[i]) * ak[i]);
+                tmem_st32(ta, t32);
               }
               tmem_wait_st();
               tc_fence_before();
