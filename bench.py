@@ -336,56 +336,94 @@ def main():
     ms_per_step = total_ms / args.steps
     value = world * T / (ms_per_step * 1e-3)
 
-    # ---- e2e through the public API with host buffers (pinned), copies inside the timed region
+    # ---- e2e through the public API with host buffers (pinned), copies inside the timed region.
+    # A serving loop: every step copies its inputs host -> device, runs kv_write + decode
+    # (+ combine) and copies out / lse back to the host. Three streams overlap the copies of
+    # neighbouring steps with the compute of the current one (inputs, outputs and host output
+    # buffers are double-buffered; events order every reuse), compute stays in step order on
+    # one stream, and the clock runs from the first copy to the last one landing on the host.
     hq = torch.from_numpy(w.q.view(np.int16)).pin_memory()
     hrows = None if w.new_rows is None else torch.from_numpy(w.new_rows.view(np.int16)).pin_memory()
     hslots = None if w.new_slots is None else torch.from_numpy(w.new_slots).pin_memory()
     hbt = torch.from_numpy(w.block_table).pin_memory()
     hsl = torch.from_numpy(w.seqlens).pin_memory()
     hidx = None if w.indices is None else torch.from_numpy(w.indices).pin_memory()
-    hout = torch.empty(T, N, 512, dtype=torch.int16).pin_memory()
-    hlse = torch.empty(T, N, dtype=torch.float32).pin_memory()
-    dq = torch.empty_like(q)
-    drows = None if rows is None else torch.empty_like(rows)
-    dslots = None if slots is None else torch.empty_like(slots)
-    dbt, dsl = torch.empty_like(bt), torch.empty_like(sl)
-    didx = None if idx is None else torch.empty_like(idx)
+    p0 = mla.mla_decode_plan(w.seqlens, c.sq, N, c.topk, c.min_splits, num_sms)
+    nb = 2
+    hout = [torch.empty(T, N, 512, dtype=torch.int16).pin_memory() for _ in range(nb)]
+    hlse = [torch.empty(T, N, dtype=torch.float32).pin_memory() for _ in range(nb)]
+    hsch = [torch.empty(p0.sched.shape, dtype=torch.int32).pin_memory() for _ in range(nb)]
+    hns = [torch.empty(p0.num_splits.shape, dtype=torch.int32).pin_memory() for _ in range(nb)]
+    dq = [torch.empty_like(q) for _ in range(nb)]
+    drows = [None if rows is None else torch.empty_like(rows) for _ in range(nb)]
+    dslots = [None if slots is None else torch.empty_like(slots) for _ in range(nb)]
+    dbt = [torch.empty_like(bt) for _ in range(nb)]
+    dsl = [torch.empty_like(sl) for _ in range(nb)]
+    didx = [None if idx is None else torch.empty_like(idx) for _ in range(nb)]
+    dsch = [torch.empty(p0.sched.shape, dtype=torch.int32, device=dev) for _ in range(nb)]
+    dns = [torch.empty(p0.num_splits.shape, dtype=torch.int32, device=dev) for _ in range(nb)]
+    dout = [torch.empty_like(out) for _ in range(nb)]
+    dlse = [torch.empty_like(lse) for _ in range(nb)]
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev() for _ in range(nb)], [ev() for _ in range(nb)], [ev() for _ in range(nb)]
+    used = [False] * nb
 
-    def e2e_step():
-        dq.view(torch.int16).copy_(hq, non_blocking=True)
-        if drows is not None:
-            drows.view(torch.int16).copy_(hrows, non_blocking=True)
-            dslots.copy_(hslots, non_blocking=True)
-        dbt.copy_(hbt, non_blocking=True)
-        dsl.copy_(hsl, non_blocking=True)
-        if didx is not None:
-            didx.copy_(hidx, non_blocking=True)
+    def e2e_step(i):
+        b = i % nb
         p = mla.mla_decode_plan(w.seqlens, c.sq, N, c.topk, c.min_splits, num_sms)
-        hs = torch.from_numpy(p.sched).pin_memory()
-        hn = torch.from_numpy(p.num_splits).pin_memory()
-        dsch = hs.to(dev, non_blocking=True)
-        dns = hn.to(dev, non_blocking=True)
-        if drows is not None:
-            mla.mla_kv_write(drows, dslots, kv, c.layout, c.page_size, stream=stream)
-        mla.mla_decode(dq, kv, c.layout, c.page_size, dbt, dsl, c.sq, c.sm_scale, dsch, dns, p.num_partitions,
-                       p.total_splits, ws, out, lse, sink=sink, indices=didx, causal=c.causal, stream=stream)
-        hout.copy_(out.view(torch.int16), non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
-        return hs.nbytes + hn.nbytes
+        assert p.sched.shape == p0.sched.shape
+        if used[b]:
+            in_done[b].synchronize()              # the pinned plan buffers of step i - 2 have been read
+        hsch[b].numpy()[...] = p.sched
+        hns[b].numpy()[...] = p.num_splits
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(comp_done[b])     # step i - 2 no longer reads these inputs
+            dq[b].view(torch.int16).copy_(hq, non_blocking=True)
+            if drows[b] is not None:
+                drows[b].view(torch.int16).copy_(hrows, non_blocking=True)
+                dslots[b].copy_(hslots, non_blocking=True)
+            dbt[b].copy_(hbt, non_blocking=True)
+            dsl[b].copy_(hsl, non_blocking=True)
+            if didx[b] is not None:
+                didx[b].copy_(hidx, non_blocking=True)
+            dsch[b].copy_(hsch[b], non_blocking=True)
+            dns[b].copy_(hns[b], non_blocking=True)
+            in_done[b].record(s_in)
+        s_comp.wait_event(in_done[b])
+        if used[b]:
+            s_comp.wait_event(out_done[b])        # out / lse of step i - 2 are on the host
+        if drows[b] is not None:
+            mla.mla_kv_write(drows[b], dslots[b], kv, c.layout, c.page_size, stream=s_comp)
+        mla.mla_decode(dq[b], kv, c.layout, c.page_size, dbt[b], dsl[b], c.sq, c.sm_scale, dsch[b], dns[b],
+                       p.num_partitions, p.total_splits, ws, dout[b], dlse[b], sink=sink, indices=didx[b],
+                       causal=c.causal, stream=s_comp)
+        comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            hout[b].copy_(dout[b].view(torch.int16), non_blocking=True)
+            hlse[b].copy_(dlse[b], non_blocking=True)
+            out_done[b].record(s_out)
+        used[b] = True
+        return hsch[b].nbytes + hns[b].nbytes
 
-    for _ in range(5):
-        e2e_step()
+    for i in range(5):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     sched_bytes = 0
-    for _ in range(args.e2e_steps):
-        sched_bytes = e2e_step()
-    torch.cuda.synchronize(dev)
+    for i in range(args.e2e_steps):
+        sched_bytes = e2e_step(i)
+    for b in range(nb):
+        out_done[b].synchronize()
     e2e_s = time.perf_counter() - t0
     if dist is not None:
         t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
+    # the last step's results must equal those of the device-timed path
+    e2e_matches = bool(torch.equal(hout[(args.e2e_steps - 1) % nb], out.view(torch.int16).cpu()))
     h2d = (w.q.nbytes + (0 if w.new_rows is None else w.new_rows.nbytes + w.new_slots.nbytes) +
            w.block_table.nbytes + w.seqlens.nbytes + (0 if w.indices is None else w.indices.nbytes) + sched_bytes)
     d2h = T * N * 512 * 2 + T * N * 4
@@ -443,8 +481,10 @@ def main():
                           "combine": statistics.mean(cmb_ms)},
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                    "steps": args.e2e_steps, "includes": "host plan, pinned H2D of q/new rows/slots/block_table/"
-                                                         "seqlens/plan, kv_write, decode, combine, D2H of out+lse"},
+                    "steps": args.e2e_steps, "matches_device_path": e2e_matches,
+                    "includes": "per step: host plan, pinned H2D of q/new rows/slots/block_table/seqlens/plan, "
+                                "kv_write, decode, combine, D2H of out+lse; copies of neighbouring steps overlap "
+                                "the current step's compute (3 streams, double-buffered, event-ordered)"},
             "gpu_launches": launches_per_step * args.steps,
             "plan": {"partitions": plan.num_partitions, "groups": plan.groups, "total_splits": plan.total_splits},
             "clocks": clocks}
