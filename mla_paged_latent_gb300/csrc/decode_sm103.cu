@@ -662,6 +662,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           }
           uint2 sc = make_uint2(0, 0);
           if (LAYOUT != 0 && valid) sc = ld_nc_v2(scp);
+          // dequantise in registers before waiting for the stage, so that only the stores
+          // remain once the PV two tiles back has released it: an fp8 chunk (16 e4m3 codes of
+          // group c/4) becomes 16 bf16 in lo/hi; a bf16 (RoPE) chunk stays in lo
+          uint4 lo[CPT], hi[CPT];
+#pragma unroll
+          for (int i = 0; i < CPT; ++i) {
+            const int c = part4 + 4 * i;
+            lo[i] = v[i];
+            hi[i] = make_uint4(0, 0, 0, 0);
+            if (LAYOUT != 0 && c < C::kNope / 16) {
+              const int grp = c >> 2;
+              const uint32_t sbyte = (grp < 4 ? (sc.x >> (8 * grp)) : (sc.y >> (8 * (grp - 4)))) & 0xFFu;
+              const float scale = valid ? ue8m0_to_f32(sbyte) : 0.f;
+              const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+              uint32_t o[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 a = e4m3x2_to_f32x2(w4[q] & 0xFFFFu);
+                const float2 b = e4m3x2_to_f32x2(w4[q] >> 16);
+                o[2 * q] = f32x2_to_bf16x2(a.x * scale, a.y * scale);
+                o[2 * q + 1] = f32x2_to_bf16x2(b.x * scale, b.y * scale);
+              }
+              lo[i] = make_uint4(o[0], o[1], o[2], o[3]);
+              hi[i] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+          }
           if (it >= 2 && !mbar_wait(bar(kv_empty(st, 4)), ((it >> 1) - 1) & 1, abort_flag, P.status)) return;
           fence_proxy_async_smem();
           if (lane == 0) {
@@ -676,29 +702,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const int c = part4 + 4 * i;
             if (LAYOUT == 0) {
               // bf16 copy: chunk c = dims [8c, 8c + 8)
-              st_shared_v4(dst + (c >> 3) * kSlab + sw128_offset(crow, (c & 7) * 8), v[i]);
+              st_shared_v4(dst + (c >> 3) * kSlab + sw128_offset(crow, (c & 7) * 8), lo[i]);
             } else if (c < C::kNope / 16) {
-              // 16 e4m3 codes of group c/4 -> 16 bf16 at dims [16c, 16c + 16)
-              const int grp = c >> 2;
-              const uint32_t sbyte = (grp < 4 ? (sc.x >> (8 * grp)) : (sc.y >> (8 * (grp - 4)))) & 0xFFu;
-              const float scale = valid ? ue8m0_to_f32(sbyte) : 0.f;
-              const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-              uint32_t o[8];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float2 a = e4m3x2_to_f32x2(w4[q] & 0xFFFFu);
-                const float2 b = e4m3x2_to_f32x2(w4[q] >> 16);
-                o[2 * q] = f32x2_to_bf16x2(a.x * scale, a.y * scale);
-                o[2 * q + 1] = f32x2_to_bf16x2(b.x * scale, b.y * scale);
-              }
-              const uint32_t sl = dst + grp * kSlab;
+              // dims [16c, 16c + 16) of slab c/4
+              const uint32_t sl = dst + (c >> 2) * kSlab;
               const int k0 = (c & 3) * 16;
-              st_shared_v4(sl + sw128_offset(crow, k0), make_uint4(o[0], o[1], o[2], o[3]));
-              st_shared_v4(sl + sw128_offset(crow, k0 + 8), make_uint4(o[4], o[5], o[6], o[7]));
+              st_shared_v4(sl + sw128_offset(crow, k0), lo[i]);
+              st_shared_v4(sl + sw128_offset(crow, k0 + 8), hi[i]);
             } else {
               // RoPE: 8 bf16 at dims [nope + 8k, nope + 8k + 8)
               const int dim = C::kNope + 8 * (c - C::kNope / 16);
-              st_shared_v4(dst + (dim >> 6) * kSlab + sw128_offset(crow, dim & 63), v[i]);
+              st_shared_v4(dst + (dim >> 6) * kSlab + sw128_offset(crow, dim & 63), lo[i]);
             }
           }
           fence_proxy_async_smem();
