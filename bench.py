@@ -197,6 +197,17 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x, dist, device="cpu"):
+    """The maximum of a per-rank scalar over all ranks (the slowest replica's
+    time); x itself when there is no process group."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def config_dict(w, args):
     c = w.cfg
     desc = {
@@ -328,11 +339,7 @@ def main():
     dec_ms = [e[1].elapsed_time(e[2]) for e in events]
     kvw_ms = [e[0].elapsed_time(e[1]) for e in events]
     cmb_ms = [e[2].elapsed_time(e[3]) for e in events]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     value = world * T / (ms_per_step * 1e-3)
 
@@ -417,11 +424,7 @@ def main():
         sched_bytes = e2e_step(i)
     for b in range(nb):
         out_done[b].synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     # the last step's results must equal those of the device-timed path
     e2e_matches = bool(torch.equal(hout[(args.e2e_steps - 1) % nb], out.view(torch.int16).cpu()))
     h2d = (w.q.nbytes + (0 if w.new_rows is None else w.new_rows.nbytes + w.new_slots.nbytes) +
