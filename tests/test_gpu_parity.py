@@ -118,6 +118,12 @@ SMALL = {
     "tail_nan_bf16": lambda: workloads.dsv3(batch=3, seqlens=(10, 70, 200), len_dist="fixed", tail_fill="nan"),
     "tail_nan_fp8": lambda: workloads.dsv4(batch=3, seqlens=(10, 70, 200), len_dist="fixed", tail_fill="nan"),
     "empty_requests": lambda: workloads.dsv4(batch=4, seqlens=(0, 65, 0, 3), len_dist="fixed", new_rows=False),
+    # the smallest page (8 TMA boxes per 64-row slab), empty requests on the bf16 TMA path,
+    # a head count that is not a multiple of 16, and the largest query-row count (32 x 128)
+    "dsv3_ps8": lambda: workloads.dsv3(batch=3, seqlens=(5, 64, 333), len_dist="fixed", page_size=8),
+    "empty_bf16": lambda: workloads.dsv3(batch=4, seqlens=(0, 65, 0, 3), len_dist="fixed", new_rows=False),
+    "heads20": lambda: workloads.dsv3(batch=2, heads=20, seqlens=(100, 700), len_dist="fixed"),
+    "rows4096": lambda: workloads.verify(batch=1, sq=32, seqlens=(200,), len_dist="fixed"),
 }
 
 
