@@ -32,7 +32,7 @@
  *  S.1111.111 is NaN, largest finite 448) and the OCP MX specification
  *  (E8M0 scale: 2^(b-127), 0xFF is NaN).
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent:
  *  - lse is natural-log and covers keys only; the sink enters only the output
  *    denominator.
  *  - An empty candidate set gives out = 0 and lse = -inf, with or without sink.

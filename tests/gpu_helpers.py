@@ -7,9 +7,9 @@ import torch
 import mla_paged_latent_gb300 as mla
 import oracle
 
-# Tolerances of the decode outputs (benchmark spec; elementwise bound
-# relaxed to 1e-2 * max(1, |ref|) because one bf16 half-ulp exceeds 1e-2 once
-# |out| > 2).
+# Tolerances of the decode outputs: max abs error 1e-2, relative L2 5e-3, lse
+# abs error 1e-3. The elementwise bound is read as 1e-2 * max(1, |ref|): one
+# bf16 half-ulp of the output alone exceeds 1e-2 once |out| > 2.
 OUT_ABS = 1e-2
 OUT_REL_L2 = 5e-3
 LSE_ABS = 1e-3

@@ -4,7 +4,7 @@ This module only draws random numbers and lays them out in the paged formats;
 it holds none of the decode arithmetic. Both the CUDA path (tests, bench) and
 the oracle consume what it produces.
 
-Workloads (shapes from the decode configurations the spec describes):
+Workloads (shapes of DeepSeek-V3/V4-style decode, speculative verify and sparse top-k batches):
   tiny    2 x 1 token, N=16, bf16 KV, L = (37, 130), page 16, values N(0,1)*0.5
   dsv3    64 x 1 token, N=128, bf16 KV, L ~ U{1024..8192}, page 64
   dsv4    128 x 1 token, N=64, fp8-448 KV (ue8m0/64, exponents U{-4..4}),
