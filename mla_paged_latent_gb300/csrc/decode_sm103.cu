@@ -24,9 +24,9 @@
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: Q once per unit, KV tiles through block_table (bf16 dense)
-//   warp 1      TMEM allocator; PV MMA issuer (one thread)
+//   warp 1      TMEM allocator; PV MMA issuer (one thread) [fp8-448: L2 prefetch]
 //   warp 2      S MMA issuer (one thread)
-//   warp 3      L2 prefetch of upcoming tiles
+//   warp 3      L2 prefetch of upcoming tiles [fp8-448: PV MMA issuer]
 //   warps 4-7   softmax (warps 4,5: one query row per thread) + O rescale + epilogue
 //   warps 8-15  converters: fp8 -> bf16 dequantisation and sparse row gathers
 #include <cstdint>
@@ -112,6 +112,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                       const __grid_constant__ CUtensorMap kv_map) {
   using C = Cfg<LAYOUT, TMA_KV>;
   constexpr int NS = C::kNslab;
+  // Warp w runs on SM sub-partition w % 4, and the softmax row threads must be warps 4 and 5
+  // (TMEM lanes 0-63 are open only to warps with w % 4 = 0, 1). The PV issuer shares
+  // sub-partition 1 with warp 5 except in the fp8-448 variant, where it runs on warp 3 and the
+  // L2 prefetch warp takes warp 1 (measured: DSV4-shaped decode 3 % faster; the sparse fp8-512
+  // variant, whose prefetch warp does per-row work, is 3 % slower that way).
+  constexpr int kPvWarp = (LAYOUT == 1) ? 3 : 1;
+  constexpr int kPrefetchWarp = (LAYOUT == 1) ? 1 : 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_addr(smem);
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mma_commit(bar(kFinal));
       mbar_wait_drain(bar(kFinal), 0);
     }
-  } else if (warp == 1) {
+  } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ PV issuer
     // O^T += V^T P^T for each tile as soon as the softmax has written P^T(j)
     // (and, for a unit's first tile, the epilogue has read the previous O^T).
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       mma_commit(bar(kFinal));
       mbar_wait_drain(bar(kFinal), 0);
     }
-  } else if (warp == 3) {
+  } else if (warp == kPrefetchWarp) {
     // ------------------------------------------------------------ L2 prefetch
     // Streams the Q rows and KV rows of upcoming tiles from HBM into L2 so that
     // the stage fills (TMA or converters) find them there. It runs ahead of the
