@@ -94,8 +94,9 @@ int mla_page_bytes(mla_kv_layout layout, int32_t page_size, int64_t* page_bytes)
  *    P = max(1, num_sms / G) partitions share the SMs.
  *  - request b has nb_b = max(1, ceil(K_b / 64)) KV blocks, K_b = topk if
  *    topk > 0 else cache_seqlens[b]; its cost is nb_b + 2.
- *  - payload = max(ceil(sum cost / P) + 4, 3) (the slack keeps the number of
- *    partitions <= P); with min_splits > 1 it is capped at
+ *  - payload = the smallest p >= p0 = max(ceil(sum cost / P), 3) with which the
+ *    greedy fill below opens at most P partitions (p0 + 4 always does, so only
+ *    p0 .. p0 + 4 are tried); with min_splits > 1 it is then capped at
  *    max(1, min_b nb_b / min_splits) + 2 (integer division), which cuts every
  *    request of >= min_splits blocks into >= min_splits splits.
  *  - partitions are filled greedily in request order; a partition that cannot

@@ -98,6 +98,7 @@ struct Cfg {
   static constexpr uint32_t kOffPLo = kOffP + (kPInStage ? 0 : 2 * kSlab);
   static constexpr uint32_t kOffMisc = kOffPLo + (kPSplit ? kSlab : 0);
   static constexpr uint32_t kSmem = kOffMisc + sizeof(Misc) + 1024;
+  static_assert(kSmem <= 232448, "shared memory budget of one CTA");
   static constexpr int kChunks = (LAYOUT == 0) ? 72 : (kNope / 16 + 8);  // 16-B chunks per stored row
   static constexpr int kChunksPerThread = kChunks / 4;
   __device__ static uint32_t stage(uint32_t base, int st) { return base + kOffStage + st * kStageBytes; }

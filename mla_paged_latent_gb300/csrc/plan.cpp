@@ -6,8 +6,9 @@
 // and I/O Contract of get_mla_metadata) — but not the rule. This file's rule:
 // requests are cut into KV blocks of 64 rows, each costing 1 plus a fixed 2 per
 // split; partitions (one per SM, or per SM group when a request needs several
-// query-row groups) are filled greedily in request order up to
-// ceil(total cost / partitions); a request that does not fit is split. The
+// query-row groups) are filled greedily in request order up to a payload, the
+// smallest one from ceil(total cost / partitions) up with which the fill needs
+// no more partitions than there are; a request that does not fit is split. The
 // include/mla_decode.h comment on mla_decode_plan states the rule in full.
 #include <algorithm>
 #include <cstdint>
@@ -34,33 +35,49 @@ PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int t
     total += nb[b] + kFixedCost;
     min_nb = std::min(min_nb, nb[b]);
   }
-  // the 2 * kFixedCost slack keeps the number of partitions <= parts
-  int64_t payload = std::max<int64_t>(cdiv(total, parts) + 2 * kFixedCost, kFixedCost + 1);
+  // Greedy fill in request order; returns the number of partitions it opens and,
+  // if out != nullptr, their sched rows and per-request split counts.
+  auto fill = [&](int64_t payload, std::vector<int32_t>* out, std::vector<int>* splits) -> int {
+    int count = 0, b = 0, blk = 0;
+    std::vector<int> sp(batch, 0);
+    while (b < batch) {
+      int64_t budget = payload;
+      const int begin_b = b, begin_blk = blk, first_split = sp[b];
+      while (b < batch && budget > kFixedCost) {
+        const int64_t remain = nb[b] - blk;
+        const int64_t take = std::min<int64_t>(remain, budget - kFixedCost);
+        budget -= take + kFixedCost;
+        sp[b] += 1;
+        blk += static_cast<int>(take);
+        if (blk == nb[b]) {
+          ++b;
+          blk = 0;
+        } else {
+          break;
+        }
+      }
+      ++count;
+      if (out) {
+        const int32_t row[8] = {begin_b, begin_blk, b, blk, first_split, 0, 0, 0};
+        out->insert(out->end(), row, row + 8);
+      }
+    }
+    if (splits) *splits = sp;
+    return count;
+  };
+  // the smallest payload from ceil(total / parts) up that needs at most `parts`
+  // partitions; ceil(total / parts) + 2 * kFixedCost always does (every closed
+  // partition is charged at least payload - kFixedCost and each continuation adds
+  // kFixedCost), so the search ends within 2 * kFixedCost + 1 fills
+  const int64_t p0 = std::max<int64_t>(cdiv(total, parts), kFixedCost + 1);
+  int64_t payload = p0;
+  while (payload < p0 + 2 * kFixedCost && fill(payload, nullptr, nullptr) > parts) ++payload;
   if (min_splits > 1 && batch > 0) {
     const int64_t cap = std::max(1, min_nb / min_splits);
     payload = std::min<int64_t>(payload, cap + kFixedCost);
   }
-  std::vector<int> splits(batch, 0);
-  int b = 0, blk = 0;
-  while (b < batch) {
-    int64_t budget = payload;
-    const int begin_b = b, begin_blk = blk, first_split = splits[b];
-    while (b < batch && budget > kFixedCost) {
-      const int64_t remain = nb[b] - blk;
-      const int64_t take = std::min<int64_t>(remain, budget - kFixedCost);
-      budget -= take + kFixedCost;
-      splits[b] += 1;
-      blk += static_cast<int>(take);
-      if (blk == nb[b]) {
-        ++b;
-        blk = 0;
-      } else {
-        break;
-      }
-    }
-    const int32_t row[8] = {begin_b, begin_blk, b, blk, first_split, 0, 0, 0};
-    res.sched.insert(res.sched.end(), row, row + 8);
-  }
+  std::vector<int> splits;
+  fill(payload, &res.sched, &splits);
   res.num_splits.assign(batch + 1, 0);
   for (int i = 0; i < batch; ++i) {
     res.num_splits[i + 1] = res.num_splits[i] + splits[i];

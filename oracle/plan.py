@@ -16,11 +16,12 @@ Rule
   K_b = topk for sparse decode and cache_seqlens[b] otherwise. An empty request
   keeps one (fully masked) block so that some CTA writes its zero output.
 * Cost of a request = nb_b + FIXED (FIXED = 2 block-equivalents of per-split
-  overhead). payload = max(ceil(sum cost / P) + 2*FIXED, FIXED + 1); the 2*FIXED
-  slack guarantees that the greedy fill below never opens more than P
-  partitions: every closed partition is charged at least payload - FIXED, each
-  continuation adds FIXED, so (P'-1)(payload - 2*FIXED) < sum cost. With min_splits > 1
-  the payload is capped at max(1, min_b nb_b // min_splits) + FIXED so that
+  overhead). payload = the smallest value p >= p0 = max(ceil(sum cost / P),
+  FIXED + 1) for which the greedy fill below opens at most P partitions;
+  p0 + 2*FIXED always qualifies (every closed partition is charged at least
+  payload - FIXED and each continuation adds FIXED, so (P'-1)(payload - 2*FIXED)
+  < sum cost), so only p0 .. p0 + 2*FIXED are tried. With min_splits > 1 the
+  payload is then capped at max(1, min_b nb_b // min_splits) + FIXED so that
   every request with at least min_splits blocks is cut into >= min_splits splits.
 * Partitions are filled greedily in request order: each segment taken costs its
   blocks + FIXED; a partition that cannot hold the rest of a request takes
@@ -52,28 +53,34 @@ def plan_split_kv(cache_seqlens, sq: int, nheads: int, topk: int, min_splits: in
     P = max(1, num_sms // G)
     nb = [max(1, _cdiv(topk if topk > 0 else L, block_rows)) for L in seqlens]
     total = sum(n + FIXED_COST for n in nb)
-    payload = max(_cdiv(total, P) + 2 * FIXED_COST, FIXED_COST + 1)
+
+    def fill(payload):
+        sched, splits = [], [0] * B
+        b, blk = 0, 0
+        while b < B:
+            budget = payload
+            begin_b, begin_blk, first_split = b, blk, splits[b]
+            while b < B and budget > FIXED_COST:
+                remain = nb[b] - blk
+                take = min(remain, budget - FIXED_COST)
+                budget -= take + FIXED_COST
+                splits[b] += 1
+                blk += take
+                if blk == nb[b]:
+                    b, blk = b + 1, 0
+                else:
+                    break
+            sched.append((begin_b, begin_blk, b, blk, first_split, 0, 0, 0))
+        return sched, splits
+
+    p0 = max(_cdiv(total, P), FIXED_COST + 1)
+    payload = p0
+    while payload < p0 + 2 * FIXED_COST and len(fill(payload)[0]) > P:
+        payload += 1
     if min_splits > 1 and B > 0:
         cap = max(1, min(nb) // min_splits)
         payload = min(payload, cap + FIXED_COST)
-
-    sched = []
-    splits = [0] * B
-    b, blk = 0, 0
-    while b < B:
-        budget = payload
-        begin_b, begin_blk, first_split = b, blk, splits[b]
-        while b < B and budget > FIXED_COST:
-            remain = nb[b] - blk
-            take = min(remain, budget - FIXED_COST)
-            budget -= take + FIXED_COST
-            splits[b] += 1
-            blk += take
-            if blk == nb[b]:
-                b, blk = b + 1, 0
-            else:
-                break
-        sched.append((begin_b, begin_blk, b, blk, first_split, 0, 0, 0))
+    sched, splits = fill(payload)
 
     num_splits = np.zeros(B + 1, dtype=np.int32)
     for i in range(B):
