@@ -93,14 +93,14 @@ int mla_page_bytes(mla_kv_layout layout, int32_t page_size, int64_t* page_bytes)
  *  - G = ceil(q_tokens_per_req*num_heads / 64) query-row groups per request;
  *    P = max(1, num_sms / G) partitions share the SMs.
  *  - request b has nb_b = max(1, ceil(K_b / 64)) KV blocks, K_b = topk if
- *    topk > 0 else cache_seqlens[b]; its cost is nb_b + 2.
- *  - payload = the smallest p >= p0 = max(ceil(sum cost / P), 3) with which the
- *    greedy fill below opens at most P partitions (p0 + 4 always does, so only
- *    p0 .. p0 + 4 are tried); with min_splits > 1 it is then capped at
- *    max(1, min_b nb_b / min_splits) + 2 (integer division), which cuts every
+ *    topk > 0 else cache_seqlens[b]; its cost is nb_b + 3.
+ *  - payload = the smallest p >= p0 = max(ceil(sum cost / P), 4) with which the
+ *    greedy fill below opens at most P partitions (p0 + 6 always does, so only
+ *    p0 .. p0 + 6 are tried); with min_splits > 1 it is then capped at
+ *    max(1, min_b nb_b / min_splits) + 3 (integer division), which cuts every
  *    request of >= min_splits blocks into >= min_splits splits.
  *  - partitions are filled greedily in request order; a partition that cannot
- *    take the rest of a request takes (budget - 2) blocks of it and closes.
+ *    take the rest of a request takes (budget - 3) blocks of it and closes.
  * Outputs (host arrays):
  *  sched [num_partitions][8] int32: begin_req, begin_blk, end_req, end_blk
  *        (exclusive, request-major order), first_split (split index of the first

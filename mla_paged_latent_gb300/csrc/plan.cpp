@@ -4,8 +4,8 @@
 // per request x heads and topk in; tile-scheduler metadata and per-request
 // split counts out ("Implementation:Sgl project Sglang Flash MLA", Signature
 // and I/O Contract of get_mla_metadata) — but not the rule. This file's rule:
-// requests are cut into KV blocks of 64 rows, each costing 1 plus a fixed 2 per
-// split; partitions (one per SM, or per SM group when a request needs several
+// requests are cut into KV blocks of 64 rows, each costing 1 plus a fixed 3 per
+// split (a unit's Q load, pipeline fill and epilogue; 3 measured best of 1-4); partitions (one per SM, or per SM group when a request needs several
 // query-row groups) are filled greedily in request order up to a payload, the
 // smallest one from ceil(total cost / partitions) up with which the fill needs
 // no more partitions than there are; a request that does not fit is split. The
@@ -18,7 +18,7 @@
 
 namespace mla {
 
-constexpr int kFixedCost = 2;
+constexpr int kFixedCost = 3;
 
 static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -15,7 +15,7 @@ Rule
 * Request b has nb_b = max(1, ceil(K_b / block_rows)) KV blocks, with
   K_b = topk for sparse decode and cache_seqlens[b] otherwise. An empty request
   keeps one (fully masked) block so that some CTA writes its zero output.
-* Cost of a request = nb_b + FIXED (FIXED = 2 block-equivalents of per-split
+* Cost of a request = nb_b + FIXED (FIXED = 3 block-equivalents of per-split
   overhead). payload = the smallest value p >= p0 = max(ceil(sum cost / P),
   FIXED + 1) for which the greedy fill below opens at most P partitions;
   p0 + 2*FIXED always qualifies (every closed partition is charged at least
@@ -38,7 +38,7 @@ from __future__ import annotations
 
 import numpy as np
 
-FIXED_COST = 2
+FIXED_COST = 3
 
 
 def _cdiv(a: int, b: int) -> int:

@@ -14,20 +14,20 @@ from oracle.plan import FIXED_COST, partition_segments, plan_split_kv
 
 def test_hand_worked_example():
     # seqlens (100, 300, 0, 64, 1000), 128 heads x 1 token -> 2 groups of 64 rows; 8 SMs -> 4 partitions
-    # blocks (2, 5, 1, 1, 16), costs (4, 7, 3, 3, 18), total 35, p0 = ceil(35/4) = 9
-    # payload 9: [req0 2 | req1 3], [req1 2 | req2 1] (budget 2 left: closes), [req3 1 | req4 4],
-    #            [req4 7], [req4 5] -> 5 partitions > 4, too small
-    # payload 10: p0 req0 (2 blocks, budget 10-4=6), req1 takes 6-2=4 blocks -> closes
-    #             p1 req1 block 4 (10-3=7), req2 (7-3=4), req3 (4-3=1) -> closes (1 <= FIXED)
-    #             p2 req4 takes 10-2=8 blocks; p3 req4 blocks 8..16 = 8 -> 4 partitions: payload 10
+    # blocks (2, 5, 1, 1, 16), FIXED 3: costs (5, 8, 4, 4, 19), total 40, p0 = ceil(40/4) = 10
+    # payload 10: [req0 2 | req1 2], [req1 3 | req2 1], [req3 1 | req4 3], [req4 7], [req4 6] -> 5 > 4
+    # payload 11: [req0 2 | req1 3], [req1 2 | req2 1], [req3 1 | req4 4], [req4 8], [req4 4] -> 5 > 4
+    # payload 12: p0 req0 (2 blocks, budget 12-5=7), req1 takes 7-3=4 blocks -> closes
+    #             p1 req1 block 4 (12-4=8), req2 (8-4=4), req3 (4-4=0) -> closes
+    #             p2 req4 takes 12-3=9 blocks; p3 req4 blocks 9..16 = 7 -> 4 partitions: payload 12
     p = plan_split_kv([100, 300, 0, 64, 1000], 1, 128, 0, 1, 8)
-    assert p["groups"] == 2 and p["payload"] == 10
+    assert p["groups"] == 2 and p["payload"] == 12
     assert list(p["blocks"]) == [2, 5, 1, 1, 16]
-    assert p["sched"][:, :5].tolist() == [[0, 0, 1, 4, 0], [1, 4, 4, 0, 1], [4, 0, 4, 8, 0], [4, 8, 5, 0, 1]]
+    assert p["sched"][:, :5].tolist() == [[0, 0, 1, 4, 0], [1, 4, 4, 0, 1], [4, 0, 4, 9, 0], [4, 9, 5, 0, 1]]
     assert list(p["num_splits"]) == [0, 1, 3, 4, 5, 7]
     segs = [partition_segments(r, p["blocks"]) for r in p["sched"]]
-    assert segs == [[(0, 0, 2, 0), (1, 0, 4, 0)], [(1, 4, 5, 1), (2, 0, 1, 0), (3, 0, 1, 0)], [(4, 0, 8, 0)],
-                    [(4, 8, 16, 1)]]
+    assert segs == [[(0, 0, 2, 0), (1, 0, 4, 0)], [(1, 4, 5, 1), (2, 0, 1, 0), (3, 0, 1, 0)], [(4, 0, 9, 0)],
+                    [(4, 9, 16, 1)]]
 
 
 def _check_invariants(p, seqlens, topk, min_splits):
