@@ -73,6 +73,11 @@ typedef enum {
 #define MLA_GROUP_ROWS 64       /* query rows (token x head) per CTA work item */
 #define MLA_WORKSPACE_HEADER 256
 #define MLA_DECODE_SKIP_COMBINE 1u  /* mla_decode flag: leave split partials in the workspace */
+/* mla_decode flag, for testing failure detection only: the decode kernel withholds
+ * the signal that its first score tile is complete, so the softmax's bounded wait
+ * runs out; every role then leaves its loop, the call completes, and the workspace
+ * status word reports MLA_STATUS_WAIT_TIMEOUT (~2 s later). Outputs are undefined. */
+#define MLA_DECODE_TEST_WITHHOLD_SIGNAL 0x80000000u
 
 typedef struct {
   int32_t num_partitions;   /* rows of sched produced */

@@ -145,7 +145,8 @@ def mla_decode_plan(cache_seqlens, q_tokens_per_req: int, num_heads: int, topk: 
 
 def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens, q_tokens_per_req: int,
                sm_scale: float, sched, num_splits, num_partitions: int, total_splits: int, workspace, out, lse,
-               sink=None, indices=None, causal: bool = False, skip_combine: bool = False, stream=None):
+               sink=None, indices=None, causal: bool = False, skip_combine: bool = False, stream=None,
+               _test_withhold_signal: bool = False):
     """Enqueue decode (+ split combine) on `stream`. All tensors on the GPU:
     q bf16 [T, N, Dqk]; kv_cache uint8 [num_pages, page_bytes]; block_table int32 [B, max_pages];
     cache_seqlens int32 [B]; sched int32 [P, 8]; num_splits int32 [B+1]; workspace uint8;
@@ -158,7 +159,8 @@ def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seql
                              block_table.shape[1], _ptr(cache_seqlens), B, q_tokens_per_req, N, float(sm_scale),
                              _ptr(sink), _ptr(indices), topk, int(bool(causal)), _ptr(sched), _ptr(num_splits),
                              num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
-                             1 if skip_combine else 0, _stream(stream)))
+                             (1 if skip_combine else 0) | (0x80000000 if _test_withhold_signal else 0),
+                             _stream(stream)))
 
 
 def mla_decode_static_workspace(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens,

@@ -249,6 +249,7 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
   p.num_partitions = num_partitions;
   p.num_work = num_partitions * groups;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.test_withhold_signal = (flags & MLA_DECODE_TEST_WITHHOLD_SIGNAL) ? 1 : 0;
 
   mla::DecodeVariant v;
   if (layout == MLA_KV_BF16_576) v = tma_kv ? mla::DecodeVariant::kBf16Tma : mla::DecodeVariant::kBf16Gather;

@@ -275,7 +275,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               qs += kSlab >> 4;
               ksd += kSlab >> 4;
             }
-            mma_commit(bar(kSFull + st));
+            // (failure-detection test: withhold the first tile's signal so that the
+            // softmax's bounded wait runs out)
+            if (!(P.test_withhold_signal && itj == 0)) mma_commit(bar(kSFull + st));
           }
           mma_commit(bar(kQEmpty));
           it += ntile;

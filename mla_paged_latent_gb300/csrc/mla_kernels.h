@@ -43,6 +43,7 @@ struct DecodeParams {
   int32_t num_partitions;
   int32_t num_work;               // num_partitions * groups
   float scale_log2;               // sm_scale * log2(e)
+  int32_t test_withhold_signal;   // MLA_DECODE_TEST_WITHHOLD_SIGNAL: skip the first S-complete commit
 };
 
 // Kernel variants: layout 0 with TMA page loads (dense), layout 0 gathered by
