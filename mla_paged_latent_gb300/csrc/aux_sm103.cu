@@ -32,11 +32,62 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= R) return;
   const int lane = threadIdx.x & 31;
+  const int64_t orow = (int64_t)b * R + row;
+  if (ns <= 4) {
+    // up to 4 splits (the common case): every load first, in one round trip to memory
+    float ls[4];
+    float4 v[4][4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      ls[s] = -INFINITY;
+      if (s < ns) {
+        ls[s] = part_lse[(int64_t)(s0 + s) * R + row];
+        const float4* src = reinterpret_cast<const float4*>(part_out + ((int64_t)(s0 + s) * R + row) * 512);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[s][k] = src[k * 32 + lane];
+      }
+    }
+    const float mx = fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3]));
+    if (mx == -INFINITY) {
+      for (int d = lane; d < 512; d += 32) out[orow * 512 + d] = 0;
+      if (lane == 0) lse[orow] = -INFINITY;
+      return;
+    }
+    float tot = 0.f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      if (s < ns) tot += expf(ls[s] - mx);
+    const float lse_tot = mx + logf(tot);
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s >= ns || ls[s] == -INFINITY) continue;
+      const float w = expf(ls[s] - lse_tot);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[4 * k + 0] += w * v[s][k].x;
+        acc[4 * k + 1] += w * v[s][k].y;
+        acc[4 * k + 2] += w * v[s][k].z;
+        acc[4 * k + 3] += w * v[s][k].w;
+      }
+    }
+    float f = 1.f;
+    if (sink != nullptr) f = 1.f / (1.f + expf(sink[row % heads] - lse_tot));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t lo = f32x2_to_bf16x2(acc[4 * k] * f, acc[4 * k + 1] * f);
+      const uint32_t hi = f32x2_to_bf16x2(acc[4 * k + 2] * f, acc[4 * k + 3] * f);
+      *reinterpret_cast<uint2*>(out + orow * 512 + (k * 32 + lane) * 4) = make_uint2(lo, hi);
+    }
+    if (lane == 0) lse[orow] = lse_tot;
+    return;
+  }
   float mx = -INFINITY;
   for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, part_lse[(int64_t)(s0 + s) * R + row]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const int64_t orow = (int64_t)b * R + row;
   if (mx == -INFINITY) {
     for (int d = lane; d < 512; d += 32) out[orow * 512 + d] = 0;
     if (lane == 0) lse[orow] = -INFINITY;
