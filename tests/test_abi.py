@@ -124,7 +124,19 @@ def test_decode_argument_validation(lib):
     assert _decode_rc(lib, sq=64, heads=128) == -2              # too many rows per request
     assert _decode_rc(lib, splits=1) == -1                      # total_splits < batch
     assert _decode_rc(lib, idx=ctypes.c_void_p(0x100000), topk=64, sq=2, heads=16) == -2
-    assert b"workspace" in lib.mla_last_error() or True
+    assert _decode_rc(lib, ws=ctypes.c_void_p(0x100010)) == -1   # workspace not 256-B aligned
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        assert _decode_rc(lib, scale=bad) == -1                 # sm_scale must be positive and finite
+    assert _decode_rc(lib, wsb=100) == -3
+    assert b"workspace" in lib.mla_last_error()                 # the message names the failed check
+
+
+def test_combine_argument_validation(lib):
+    fake = ctypes.c_void_p(0x100000)
+    assert lib.mla_combine(None, fake, fake, 2, 16, 16, None, fake, fake, None) == -1      # NULL part_out
+    assert lib.mla_combine(fake, fake, fake, 2, 20, 16, None, fake, fake, None) == -1      # rows % heads != 0
+    assert lib.mla_combine(fake, fake, fake, 0, 16, 16, None, fake, fake, None) == -1      # batch < 1
+    assert lib.mla_combine(ctypes.c_void_p(0x100004), fake, fake, 2, 16, 16, None, fake, fake, None) == -1
 
 
 def test_kv_write_and_gather_validation(lib):
