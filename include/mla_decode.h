@@ -101,9 +101,12 @@ int mla_page_bytes(mla_kv_layout layout, int32_t page_size, int64_t* page_bytes)
  *    topk > 0 else cache_seqlens[b]; its cost is nb_b + 3.
  *  - payload = the smallest p >= p0 = max(ceil(sum cost / P), 4) with which the
  *    greedy fill below opens at most P partitions (p0 + 6 always does, so only
- *    p0 .. p0 + 6 are tried); with min_splits > 1 it is then capped at
- *    max(1, min_b nb_b / min_splits) + 3 (integer division), which cuts every
- *    request of >= min_splits blocks into >= min_splits splits.
+ *    p0 .. p0 + 6 are tried).
+ *  - with min_splits = k > 1, let n = the fewest blocks of a request that has
+ *    >= k blocks; cap = max(1, (n - 1) / (k - 1)) + 3 (integer division) cuts
+ *    every such request into >= k splits. If cap < payload, the payload becomes
+ *    the p in (cap - 64, cap], p > 3, with the fewest ceil(partitions(p) / P) * p
+ *    (ties: the larger p), partitions(p) being the count the fill opens.
  *  - partitions are filled greedily in request order; a partition that cannot
  *    take the rest of a request takes (budget - 3) blocks of it and closes.
  * Outputs (host arrays):

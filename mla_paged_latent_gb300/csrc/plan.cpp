@@ -28,12 +28,12 @@ PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int t
   const int parts = std::max(1, num_sms / groups);
   std::vector<int> nb(batch);
   int64_t total = 0;
-  int min_nb = 1 << 30;
+  int min_nb = 1 << 30;  // fewest blocks of a request with at least min_splits blocks
   for (int b = 0; b < batch; ++b) {
     const int64_t K = topk > 0 ? topk : std::max<int32_t>(seqlens[b], 0);
     nb[b] = static_cast<int>(std::max<int64_t>(1, cdiv(K, kBlockRows)));
     total += nb[b] + kFixedCost;
-    min_nb = std::min(min_nb, nb[b]);
+    if (nb[b] >= min_splits) min_nb = std::min(min_nb, nb[b]);
   }
   // Greedy fill in request order; returns the number of partitions it opens and,
   // if out != nullptr, their sched rows and per-request split counts.
@@ -72,9 +72,23 @@ PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int t
   const int64_t p0 = std::max<int64_t>(cdiv(total, parts), kFixedCost + 1);
   int64_t payload = p0;
   while (payload < p0 + 2 * kFixedCost && fill(payload, nullptr, nullptr) > parts) ++payload;
-  if (min_splits > 1 && batch > 0) {
-    const int64_t cap = std::max(1, min_nb / min_splits);
-    payload = std::min<int64_t>(payload, cap + kFixedCost);
+  if (min_splits > 1 && min_nb < (1 << 30)) {
+    // segments of at most s blocks cut n >= min_nb blocks into ceil(n / s) >= min_splits
+    // pieces when s <= (min_nb - 1) / (min_splits - 1)
+    const int64_t cap = std::max(1, (min_nb - 1) / (min_splits - 1)) + kFixedCost;
+    if (cap < payload) {
+      // several waves of partitions: the payload up to the cap with the fewest
+      // waves x payload (ties: the larger payload)
+      int64_t best = cap, best_span = -1;
+      for (int64_t p = cap; p > kFixedCost && p > cap - 64; --p) {
+        const int64_t span = cdiv(fill(p, nullptr, nullptr), parts) * p;
+        if (best_span < 0 || span < best_span) {
+          best = p;
+          best_span = span;
+        }
+      }
+      payload = best;
+    }
   }
   std::vector<int> splits;
   fill(payload, &res.sched, &splits);

@@ -20,9 +20,14 @@ Rule
   FIXED + 1) for which the greedy fill below opens at most P partitions;
   p0 + 2*FIXED always qualifies (every closed partition is charged at least
   payload - FIXED and each continuation adds FIXED, so (P'-1)(payload - 2*FIXED)
-  < sum cost), so only p0 .. p0 + 2*FIXED are tried. With min_splits > 1 the
-  payload is then capped at max(1, min_b nb_b // min_splits) + FIXED so that
-  every request with at least min_splits blocks is cut into >= min_splits splits.
+  < sum cost), so only p0 .. p0 + 2*FIXED are tried.
+* With min_splits = k > 1: segments of at most s blocks cut a request of n
+  blocks into >= ceil(n / s) pieces, which is >= k when s <= (n - 1) // (k - 1).
+  So with n_min = the fewest blocks of a request that has >= k blocks, the cap
+  is max(1, (n_min - 1) // (k - 1)) + FIXED. If the cap is below the payload
+  above (the plan then needs several waves of P partitions), the payload is the
+  value p in (cap - 64, cap], p > FIXED, with the smallest ceil(count(p) / P) * p,
+  ties going to the larger p (count(p) = partitions the fill opens with p).
 * Partitions are filled greedily in request order: each segment taken costs its
   blocks + FIXED; a partition that cannot hold the rest of a request takes
   (budget - FIXED) blocks of it and closes. Partitions are opened until every
@@ -77,9 +82,18 @@ def plan_split_kv(cache_seqlens, sq: int, nheads: int, topk: int, min_splits: in
     payload = p0
     while payload < p0 + 2 * FIXED_COST and len(fill(payload)[0]) > P:
         payload += 1
-    if min_splits > 1 and B > 0:
-        cap = max(1, min(nb) // min_splits)
-        payload = min(payload, cap + FIXED_COST)
+    long_enough = [n for n in nb if n >= min_splits]
+    if min_splits > 1 and long_enough:
+        cap = max(1, (min(long_enough) - 1) // (min_splits - 1)) + FIXED_COST
+        if cap < payload:
+            best, best_span = cap, None
+            p = cap
+            while p > FIXED_COST and p > cap - 64:
+                span = _cdiv(len(fill(p)[0]), P) * p
+                if best_span is None or span < best_span:
+                    best, best_span = p, span
+                p -= 1
+            payload = best
     sched, splits = fill(payload)
 
     num_splits = np.zeros(B + 1, dtype=np.int32)
