@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ num_splits, int R, int heads,
                                                       const float* __restrict__ sink, uint16_t* __restrict__ out,
                                                       float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.y;
   const int s0 = num_splits[b];
   const int ns = num_splits[b + 1] - s0;
@@ -157,6 +159,8 @@ __global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restric
                                                        const int32_t* __restrict__ slots, int n,
                                                        uint8_t* __restrict__ kv, int layout, int64_t num_pages,
                                                        int page_size, int64_t page_bytes) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= n) return;
@@ -205,6 +209,8 @@ __global__ void __launch_bounds__(128) kv_gather_kernel(const uint8_t* __restric
                                                         int64_t num_pages, int page_size, int64_t page_bytes,
                                                         const int32_t* __restrict__ bt_row, int max_pages,
                                                         int length, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (j >= length) return;
@@ -244,23 +250,22 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
                            cudaStream_t stream) {
   if (batch <= 0 || rows_per_req <= 0) return cudaSuccess;
   dim3 grid((rows_per_req + 7) / 8, batch);
-  combine_kernel<<<grid, 256, 0, stream>>>(part_out, part_lse, num_splits, rows_per_req, heads, sink, out, lse);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(256), 0, stream, part_out, part_lse, num_splits, rows_per_req, heads,
+                    sink, out, lse);
 }
 
 cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout,
                             int64_t num_pages, int page_size, int64_t page_bytes, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  kv_write_kernel<<<(n + 3) / 4, 128, 0, stream>>>(rows, slots, n, kv, layout, num_pages, page_size, page_bytes);
-  return cudaGetLastError();
+  return launch_pdl(kv_write_kernel, dim3((n + 3) / 4), dim3(128), 0, stream, rows, slots, n, kv, layout, num_pages,
+                    page_size, page_bytes);
 }
 
 cudaError_t launch_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
                              const int32_t* bt_row, int max_pages, int length, float* out, cudaStream_t stream) {
   if (length <= 0) return cudaSuccess;
-  kv_gather_kernel<<<(length + 3) / 4, 128, 0, stream>>>(kv, layout, num_pages, page_size, page_bytes, bt_row,
-                                                         max_pages, length, out);
-  return cudaGetLastError();
+  return launch_pdl(kv_gather_kernel, dim3((length + 3) / 4), dim3(128), 0, stream, kv, layout, num_pages, page_size,
+                    page_bytes, bt_row, max_pages, length, out);
 }
 
 }  // namespace mla

@@ -161,6 +161,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the setup above overlaps the previous kernel's tail; nothing is read before this
+  pdl_trigger();
+  pdl_wait();
   const uint32_t tmem = misc->tmem_base;
   const uint32_t tmem_o = tmem;          // O^T: 4 blocks x 64 columns
   const uint32_t tmem_s = tmem + 256;    // S: 2 buffers x 64 columns
@@ -758,8 +761,7 @@ static cudaError_t launch_variant(const DecodeParams& p, const CUtensorMap& q_ma
   const size_t smem = Cfg<LAYOUT, TMA_KV>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kDecodeThreads, smem, stream>>>(p, q_map, kv_map);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kDecodeThreads), smem, stream, p, q_map, kv_map);
 }
 
 cudaError_t launch_decode(DecodeVariant v, const DecodeParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,

@@ -73,6 +73,27 @@ struct PlanResult {
   int total_splits = 0;
   int max_splits = 0;
 };
+#ifdef __CUDACC__
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on `stream` drains (hiding the launch gap); every
+// kernel of this library calls pdl_wait() before it reads its inputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+#endif
+
 PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int topk, int min_splits, int num_sms);
 
 }  // namespace mla
