@@ -24,9 +24,9 @@
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: Q once per unit, KV tiles through block_table (bf16 dense)
-//   warp 1      TMEM allocator; PV MMA issuer (one thread) [fp8-448: L2 prefetch]
+//   warp 1      TMEM allocator; L2 prefetch of upcoming tiles [layout 2 and bf16 gather: PV issuer]
 //   warp 2      S MMA issuer (one thread)
-//   warp 3      L2 prefetch of upcoming tiles [fp8-448: PV MMA issuer]
+//   warp 3      PV MMA issuer (one thread) [layout 2 and bf16 gather: L2 prefetch]
 //   warps 4-7   softmax (warps 4,5: one query row per thread) + O rescale + epilogue
 //   warps 8-15  converters: fp8 -> bf16 dequantisation and sparse row gathers
 #include <cstdint>
@@ -114,12 +114,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   using C = Cfg<LAYOUT, TMA_KV>;
   constexpr int NS = C::kNslab;
   // Warp w runs on SM sub-partition w % 4, and the softmax row threads must be warps 4 and 5
-  // (TMEM lanes 0-63 are open only to warps with w % 4 = 0, 1). The PV issuer shares
-  // sub-partition 1 with warp 5 except in the fp8-448 variant, where it runs on warp 3 and the
-  // L2 prefetch warp takes warp 1 (measured: DSV4-shaped decode 3 % faster; the sparse fp8-512
-  // variant, whose prefetch warp does per-row work, is 3 % slower that way).
-  constexpr int kPvWarp = (LAYOUT == 1) ? 3 : 1;
-  constexpr int kPrefetchWarp = (LAYOUT == 1) ? 1 : 3;
+  // (TMEM lanes 0-63 are open only to warps with w % 4 = 0, 1). The PV issuer runs on warp 3,
+  // away from softmax warp 5, and the L2 prefetch warp takes warp 1 (measured: DSV4-shaped
+  // decode 3 % faster, DSV3-shaped 0.5 %, verify 1.3 %). The sparse variants keep the PV
+  // issuer on warp 1: their prefetch warp does per-row work and they were 3 % slower.
+  constexpr int kPvWarp = (LAYOUT == 1 || TMA_KV) ? 3 : 1;
+  constexpr int kPrefetchWarp = (LAYOUT == 1 || TMA_KV) ? 1 : 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_addr(smem);
