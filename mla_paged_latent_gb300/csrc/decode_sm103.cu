@@ -374,15 +374,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             __nanosleep(256);
           }
           if (sparse) {
-            for (int k = lane; k < kBlockRows; k += 32) {
-              const int kk = j * kBlockRows + k;
-              const int pos = kk < P.topk ? P.indices[static_cast<int64_t>(tok) * P.topk + kk] : -1;
-              if (pos < 0 || pos >= L) continue;
-              const int pi = pos >> P.log2_ps;
-              const int page = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
-              if (page < 0 || page >= P.num_pages) continue;
-              const int off = pos & (P.page_size - 1);
-              const uint8_t* pg = P.kv + static_cast<int64_t>(page) * P.page_bytes;
+            // two rows per lane: both indices, then both pages, then the prefetches
+            int pos[2], page[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int kk = j * kBlockRows + lane + 32 * h;
+              pos[h] = kk < P.topk ? P.indices[static_cast<int64_t>(tok) * P.topk + kk] : -1;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              page[h] = -1;
+              if (pos[h] < 0 || pos[h] >= L) continue;
+              const int pi = pos[h] >> P.log2_ps;
+              page[h] = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (page[h] < 0 || page[h] >= P.num_pages) continue;
+              const int off = pos[h] & (P.page_size - 1);
+              const uint8_t* pg = P.kv + static_cast<int64_t>(page[h]) * P.page_bytes;
               prefetch_l2_bulk(pg + static_cast<int64_t>(off) * P.row_bytes, P.row_bytes);
               if (LAYOUT != 0) {
                 const uintptr_t sa = reinterpret_cast<uintptr_t>(pg + static_cast<int64_t>(P.page_size) * P.row_bytes +
@@ -638,31 +648,39 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (*abort_flag) return;
         const int L = P.seqlens[r];
         const int tok = r * P.sq + (g * kGroupRows) / P.heads;   // sparse: the group's token
-        for (int j = lo; j < hi; ++j, ++it) {
-          const int st = it & 1;
-          int pos;
-          bool valid;
+        // The address chain of a row (top-k index -> block_table entry -> row) runs two
+        // tiles ahead of the conversion: the index of tile j + 2 and the page of tile j + 1
+        // are loaded while tile j is converted, so only a unit's first tile waits for them.
+        auto row_pos = [&](int j) -> int {  // KV position of this thread's row of tile j, or -1
+          if (j >= hi) return -1;
           if (sparse) {
             const int kk = j * kBlockRows + crow;
-            pos = kk < P.topk ? P.indices[(int64_t)tok * P.topk + kk] : -1;
-            valid = pos >= 0 && pos < L;
-          } else {
-            pos = j * kBlockRows + crow;
-            valid = pos < L;
+            return kk < P.topk ? P.indices[(int64_t)tok * P.topk + kk] : -1;
           }
+          return j * kBlockRows + crow;
+        };
+        auto row_page = [&](int pos) -> int {  // its page; -1 if no row, -2 if the entry is bad
+          if (pos < 0 || pos >= L) return -1;
+          const int pi = pos >> P.log2_ps;
+          const int page = pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1;
+          return (page < 0 || page >= P.num_pages) ? -2 : page;
+        };
+        int pos_a = row_pos(lo), pos_b = row_pos(lo + 1);
+        int page_a = row_page(pos_a);
+        for (int j = lo; j < hi; ++j, ++it) {
+          const int st = it & 1;
+          const int pos = pos_a, page = page_a;
+          pos_a = pos_b;
+          page_a = row_page(pos_b);
+          pos_b = row_pos(j + 2);
+          bool valid = page >= 0;
+          if (page == -2 && part4 == 0) atomicOr(P.status, 2u);
           const uint8_t* rowp = nullptr;
           const uint8_t* scp = nullptr;
           if (valid) {
-            const int pi = pos >> P.log2_ps;
-            const int page = pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1;
-            if (page < 0 || page >= P.num_pages) {
-              if (part4 == 0) atomicOr(P.status, 2u);
-              valid = false;
-            } else {
-              const int off = pos & (P.page_size - 1);
-              rowp = P.kv + (int64_t)page * P.page_bytes + (int64_t)off * P.row_bytes;
-              scp = P.kv + (int64_t)page * P.page_bytes + (int64_t)P.page_size * P.row_bytes + off * 8;
-            }
+            const int off = pos & (P.page_size - 1);
+            rowp = P.kv + (int64_t)page * P.page_bytes + (int64_t)off * P.row_bytes;
+            scp = P.kv + (int64_t)page * P.page_bytes + (int64_t)P.page_size * P.row_bytes + off * 8;
           }
           const unsigned bal = __ballot_sync(0xffffffffu, valid && part4 == 0);
           // issue this tile's global loads first, then wait for the stage to be free
