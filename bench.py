@@ -360,28 +360,43 @@ def main():
     # neighbouring steps with the compute of the current one (inputs, outputs and host output
     # buffers are double-buffered; events order every reuse), compute stays in step order on
     # one stream, and the clock runs from the first copy to the last one landing on the host.
-    hq = torch.from_numpy(w.q.view(np.int16)).pin_memory()
-    hrows = None if w.new_rows is None else torch.from_numpy(w.new_rows.view(np.int16)).pin_memory()
-    hslots = None if w.new_slots is None else torch.from_numpy(w.new_slots).pin_memory()
-    hbt = torch.from_numpy(w.block_table).pin_memory()
-    hsl = torch.from_numpy(w.seqlens).pin_memory()
-    hidx = None if w.indices is None else torch.from_numpy(w.indices).pin_memory()
+    # All of a step's inputs live in one pinned host buffer and move in one copy; out and
+    # lse come back in one copy too (the device tensors are views into packed buffers).
     p0 = mla.mla_decode_plan(w.seqlens, c.sq, N, c.topk, c.min_splits, num_sms)
     nb = 2
-    hout = [torch.empty(T, N, 512, dtype=torch.int16).pin_memory() for _ in range(nb)]
-    hlse = [torch.empty(T, N, dtype=torch.float32).pin_memory() for _ in range(nb)]
-    hsch = [torch.empty(p0.sched.shape, dtype=torch.int32).pin_memory() for _ in range(nb)]
-    hns = [torch.empty(p0.num_splits.shape, dtype=torch.int32).pin_memory() for _ in range(nb)]
-    dq = [torch.empty_like(q) for _ in range(nb)]
-    drows = [None if rows is None else torch.empty_like(rows) for _ in range(nb)]
-    dslots = [None if slots is None else torch.empty_like(slots) for _ in range(nb)]
-    dbt = [torch.empty_like(bt) for _ in range(nb)]
-    dsl = [torch.empty_like(sl) for _ in range(nb)]
-    didx = [None if idx is None else torch.empty_like(idx) for _ in range(nb)]
-    dsch = [torch.empty(p0.sched.shape, dtype=torch.int32, device=dev) for _ in range(nb)]
-    dns = [torch.empty(p0.num_splits.shape, dtype=torch.int32, device=dev) for _ in range(nb)]
-    dout = [torch.empty_like(out) for _ in range(nb)]
-    dlse = [torch.empty_like(lse) for _ in range(nb)]
+    in_fields = [("q", w.q.view(np.int16)), ("rows", None if w.new_rows is None else w.new_rows.view(np.int16)),
+                 ("slots", w.new_slots), ("bt", w.block_table), ("sl", w.seqlens), ("idx", w.indices),
+                 ("sched", p0.sched), ("ns", p0.num_splits)]
+    in_off, in_bytes = {}, 0
+    for name, arr in in_fields:
+        if arr is not None:
+            in_off[name] = (in_bytes, arr.nbytes, arr.dtype, arr.shape)
+            in_bytes += (arr.nbytes + 255) // 256 * 256
+    res_fields = [("out", T * N * 512 * 2, np.int16, (T, N, 512)), ("lse", T * N * 4, np.float32, (T, N))]
+    res_off, res_bytes = {}, 0
+    for name, n, dt, shp in res_fields:
+        res_off[name] = (res_bytes, n, np.dtype(dt), shp)
+        res_bytes += (n + 255) // 256 * 256
+    tdt = {np.dtype(np.int16): torch.int16, np.dtype(np.int32): torch.int32, np.dtype(np.float32): torch.float32}
+
+    def view(buf, off, name):
+        o, n, dt, shp = off[name]
+        return buf[o:o + n].view(tdt[np.dtype(dt)]).view(shp)
+
+    hin = [torch.empty(in_bytes, dtype=torch.uint8).pin_memory() for _ in range(nb)]
+    din = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(nb)]
+    hres = [torch.empty(res_bytes, dtype=torch.uint8).pin_memory() for _ in range(nb)]
+    dres = [torch.empty(res_bytes, dtype=torch.uint8, device=dev) for _ in range(nb)]
+    for b in range(nb):
+        for name, arr in in_fields:
+            if arr is not None and name not in ("sched", "ns"):
+                view(hin[b], in_off, name).numpy()[...] = arr
+    dv = [{name: view(din[b], in_off, name) for name in in_off} for b in range(nb)]
+    hsch = [view(hin[b], in_off, "sched").numpy() for b in range(nb)]
+    hns = [view(hin[b], in_off, "ns").numpy() for b in range(nb)]
+    dout = [view(dres[b], res_off, "out").view(torch.bfloat16) for b in range(nb)]
+    dlse = [view(dres[b], res_off, "lse") for b in range(nb)]
+    hout = [view(hres[b], res_off, "out") for b in range(nb)]
     s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev = lambda: torch.cuda.Event()
     in_done, comp_done, out_done = [ev() for _ in range(nb)], [ev() for _ in range(nb)], [ev() for _ in range(nb)]
@@ -392,55 +407,43 @@ def main():
         p = mla.mla_decode_plan(w.seqlens, c.sq, N, c.topk, c.min_splits, num_sms)
         assert p.sched.shape == p0.sched.shape
         if used[b]:
-            in_done[b].synchronize()              # the pinned plan buffers of step i - 2 have been read
-        hsch[b].numpy()[...] = p.sched
-        hns[b].numpy()[...] = p.num_splits
+            in_done[b].synchronize()              # the pinned inputs of step i - 2 have been read
+        hsch[b][...] = p.sched
+        hns[b][...] = p.num_splits
+        d = dv[b]
         with torch.cuda.stream(s_in):
             if used[b]:
                 s_in.wait_event(comp_done[b])     # step i - 2 no longer reads these inputs
-            dq[b].view(torch.int16).copy_(hq, non_blocking=True)
-            if drows[b] is not None:
-                drows[b].view(torch.int16).copy_(hrows, non_blocking=True)
-                dslots[b].copy_(hslots, non_blocking=True)
-            dbt[b].copy_(hbt, non_blocking=True)
-            dsl[b].copy_(hsl, non_blocking=True)
-            if didx[b] is not None:
-                didx[b].copy_(hidx, non_blocking=True)
-            dsch[b].copy_(hsch[b], non_blocking=True)
-            dns[b].copy_(hns[b], non_blocking=True)
+            din[b].copy_(hin[b], non_blocking=True)
             in_done[b].record(s_in)
         s_comp.wait_event(in_done[b])
         if used[b]:
             s_comp.wait_event(out_done[b])        # out / lse of step i - 2 are on the host
-        if drows[b] is not None:
-            mla.mla_kv_write(drows[b], dslots[b], kv, c.layout, c.page_size, stream=s_comp)
-        mla.mla_decode(dq[b], kv, c.layout, c.page_size, dbt[b], dsl[b], c.sq, c.sm_scale, dsch[b], dns[b],
-                       p.num_partitions, p.total_splits, ws, dout[b], dlse[b], sink=sink, indices=didx[b],
-                       causal=c.causal, stream=s_comp)
+        if "rows" in d:
+            mla.mla_kv_write(d["rows"].view(torch.bfloat16), d["slots"], kv, c.layout, c.page_size, stream=s_comp)
+        mla.mla_decode(d["q"].view(torch.bfloat16), kv, c.layout, c.page_size, d["bt"], d["sl"], c.sq, c.sm_scale,
+                       d["sched"], d["ns"], p.num_partitions, p.total_splits, ws, dout[b], dlse[b], sink=sink,
+                       indices=d.get("idx"), causal=c.causal, stream=s_comp)
         comp_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[b])
-            hout[b].copy_(dout[b].view(torch.int16), non_blocking=True)
-            hlse[b].copy_(dlse[b], non_blocking=True)
+            hres[b].copy_(dres[b], non_blocking=True)
             out_done[b].record(s_out)
         used[b] = True
-        return hsch[b].nbytes + hns[b].nbytes
 
     for i in range(5):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    sched_bytes = 0
     for i in range(args.e2e_steps):
-        sched_bytes = e2e_step(i)
+        e2e_step(i)
     for b in range(nb):
         out_done[b].synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     # the last step's results must equal those of the device-timed path
     e2e_matches = bool(torch.equal(hout[(args.e2e_steps - 1) % nb], out.view(torch.int16).cpu()))
-    h2d = (w.q.nbytes + (0 if w.new_rows is None else w.new_rows.nbytes + w.new_slots.nbytes) +
-           w.block_table.nbytes + w.seqlens.nbytes + (0 if w.indices is None else w.indices.nbytes) + sched_bytes)
-    d2h = T * N * 512 * 2 + T * N * 4
+    h2d = in_bytes   # the packed inputs (256-B aligned fields), copied every step
+    d2h = res_bytes
     e2e_value = world * T * args.e2e_steps / e2e_s
 
     if rank != 0:
@@ -496,9 +499,10 @@ def main():
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "steps": args.e2e_steps, "matches_device_path": e2e_matches,
-                    "includes": "per step: host plan, pinned H2D of q/new rows/slots/block_table/seqlens/plan, "
-                                "kv_write, decode, combine, D2H of out+lse; copies of neighbouring steps overlap "
-                                "the current step's compute (3 streams, double-buffered, event-ordered)"},
+                    "includes": "per step: host plan, one pinned H2D copy of the packed q/new rows/slots/"
+                                "block_table/seqlens/indices/plan, kv_write, decode, combine, one D2H copy of "
+                                "out+lse; copies of neighbouring steps overlap the current step's compute "
+                                "(3 streams, double-buffered, event-ordered)"},
             "gpu_launches": launches_per_step * args.steps,
             "plan": {"partitions": plan.num_partitions, "groups": plan.groups, "total_splits": plan.total_splits},
             "clocks": clocks}

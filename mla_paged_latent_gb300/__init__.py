@@ -56,6 +56,8 @@ STATIC_WORKSPACE_BYTES = 64 << 20
 def load(path: str | None = None):
     """Load the compiled library (raises if it has not been built)."""
     global _lib
+    if _lib is not None and path is None:
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
@@ -89,16 +91,14 @@ def _check(rc: int):
 
 
 def _ptr(t):
-    if t is None:
-        return None
-    return ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
-    import torch
     if stream is None:
+        import torch
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _require_cuda(*tensors):
@@ -133,14 +133,21 @@ def mla_decode_plan(cache_seqlens, q_tokens_per_req: int, num_heads: int, topk: 
         import torch
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     info = _PlanInfo()
-    _check(lib.mla_decode_plan(sl.ctypes.data_as(ctypes.c_void_p), sl.shape[0], q_tokens_per_req, num_heads, topk,
-                               min_splits, num_sms, None, 0, None, ctypes.byref(info)))
-    sched = np.zeros((info.num_partitions, 8), dtype=np.int32)
-    ns = np.zeros(sl.shape[0] + 1, dtype=np.int32)
-    _check(lib.mla_decode_plan(sl.ctypes.data_as(ctypes.c_void_p), sl.shape[0], q_tokens_per_req, num_heads, topk,
-                               min_splits, num_sms, sched.ctypes.data_as(ctypes.c_void_p), info.num_partitions,
-                               ns.ctypes.data_as(ctypes.c_void_p), ctypes.byref(info)))
-    return Plan(sched, ns, info.num_partitions, info.groups, info.total_splits, info.max_splits, info.workspace_bytes)
+    ns = np.empty(sl.shape[0] + 1, dtype=np.int32)
+    # one call with room for a partition per SM x 4; the rare larger plan reports its size
+    # (MLA_ERR_CAPACITY) and is made again into a buffer of that size
+    cap = 4 * int(num_sms)
+    while True:
+        sched = np.empty((cap, 8), dtype=np.int32)
+        rc = lib.mla_decode_plan(sl.ctypes.data, sl.shape[0], q_tokens_per_req, num_heads, topk, min_splits, num_sms,
+                                 sched.ctypes.data, cap, ns.ctypes.data, ctypes.byref(info))
+        if rc == -6 and info.num_partitions > cap:
+            cap = info.num_partitions
+            continue
+        _check(rc)
+        break
+    return Plan(sched[:info.num_partitions], ns, info.num_partitions, info.groups, info.total_splits, info.max_splits,
+                info.workspace_bytes)
 
 
 def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens, q_tokens_per_req: int,

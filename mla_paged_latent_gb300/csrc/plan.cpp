@@ -37,9 +37,10 @@ PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int t
   }
   // Greedy fill in request order; returns the number of partitions it opens and,
   // if out != nullptr, their sched rows and per-request split counts.
+  std::vector<int> sp(batch);  // per-request split counts of the current fill (reused)
   auto fill = [&](int64_t payload, std::vector<int32_t>* out, std::vector<int>* splits) -> int {
     int count = 0, b = 0, blk = 0;
-    std::vector<int> sp(batch, 0);
+    std::fill(sp.begin(), sp.end(), 0);
     while (b < batch) {
       int64_t budget = payload;
       const int begin_b = b, begin_blk = blk, first_split = sp[b];
