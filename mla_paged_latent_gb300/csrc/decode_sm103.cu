@@ -75,7 +75,7 @@ struct Misc {
   int progress;  // tiles whose stage fill has been issued (throttles the L2 prefetch warp)
   int pad0;
   float alpha[2][64];  // per stage: tile j+1 must not overwrite what tile j's rescale reads
-  float inv[64];
+  alignas(16) float inv[64];
   float lse2[64];
   uint8_t mask[2][8];  // sparse / gathered row validity per stage, one byte per 8 rows
 };
@@ -607,23 +607,48 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
         if (wait(bar(kOFull), u & 1)) {
           tc_fence_after();
+          // row (query) qr of this unit goes to out[r * R + g * 64 + qr] (bf16) or to the
+          // split partial part_out[sg * R + g * 64 + qr] (fp32); this thread writes value
+          // dim blk * 128 + wt of each row, so consecutive rows are 512 elements apart
+          const int64_t row0 = (nsplit == 1 ? (int64_t)r : (int64_t)sg) * R + g * kGroupRows;
+          const float4* inv4 = reinterpret_cast<const float4*>(misc->inv);
           for (int blk = 0; blk < 4; ++blk) {
             const int d = blk * 128 + wt;
             for (int c = 0; c < nq; c += 16) {
               uint32_t t16[16];
               tmem_ld16(tmem_o + lane_off + blk * 64 + c, t16);
-              tmem_wait_ld();
+              float iv[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int qr = c + i;
-                if (qr >= rows_g) break;
-                const float v = __uint_as_float(t16[i]) * misc->inv[qr];
-                const int64_t flat = (int64_t)r * R + g * kGroupRows + qr;
-                if (nsplit == 1) {
-                  const uint32_t b = f32x2_to_bf16x2(v, 0.f);
-                  P.out[flat * 512 + d] = static_cast<uint16_t>(b & 0xFFFFu);
+              for (int k = 0; k < 4; ++k) {
+                const float4 f = inv4[(c >> 2) + k];
+                iv[4 * k] = f.x;
+                iv[4 * k + 1] = f.y;
+                iv[4 * k + 2] = f.z;
+                iv[4 * k + 3] = f.w;
+              }
+              tmem_wait_ld();
+              const int nrow = rows_g - c < 16 ? rows_g - c : 16;
+              if (nsplit == 1) {
+                uint16_t* o = P.out + (row0 + c) * 512 + d;
+                if (nrow == 16) {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    o[i * 512] = static_cast<uint16_t>(f32x2_to_bf16x2(__uint_as_float(t16[i]) * iv[i], 0.f));
                 } else {
-                  P.part_out[((int64_t)sg * R + g * kGroupRows + qr) * 512 + d] = v;
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    if (i < nrow)
+                      o[i * 512] = static_cast<uint16_t>(f32x2_to_bf16x2(__uint_as_float(t16[i]) * iv[i], 0.f));
+                }
+              } else {
+                float* o = P.part_out + (row0 + c) * 512 + d;
+                if (nrow == 16) {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) o[i * 512] = __uint_as_float(t16[i]) * iv[i];
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 16; ++i)
+                    if (i < nrow) o[i * 512] = __uint_as_float(t16[i]) * iv[i];
                 }
               }
             }
