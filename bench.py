@@ -350,6 +350,34 @@ def main():
     dec_ms = [e[1].elapsed_time(e[2]) for e in bd]
     kvw_ms = [e[0].elapsed_time(e[1]) for e in bd]
     cmb_ms = [e[2].elapsed_time(e[3]) for e in bd]
+
+    # The fused RMSNorm + RoPE + write of the same new rows (raw rows in, cache rows out), timed
+    # alone. It rewrites those slots; the e2e loop below writes them back with mla_kv_write.
+    kvnr = None
+    if rows is not None:
+        nr = int(w.new_rows.shape[0])
+        kpos = np.concatenate([np.arange(int(L) - c.sq, int(L)) for L in w.seqlens]).astype(np.int32)
+        max_pos = int(w.seqlens.max()) + 1
+        theta = np.outer(np.arange(max_pos), 10000.0 ** (-np.arange(32) / 32.0))
+        ftab = np.zeros((max_pos, 64), np.float32)
+        ftab[:, 0::2], ftab[:, 1::2] = np.cos(theta), np.sin(theta)
+        d_pos, d_f = torch.from_numpy(kpos).to(dev), torch.from_numpy(ftab).to(dev)
+        d_w = torch.ones(512, dtype=torch.bfloat16, device=dev)
+        nk = []
+        for k in range(nbd):
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            mla.mla_kv_write_norm_rope(rows, slots, d_pos, d_w, 1e-6, d_f, kv, c.layout, c.page_size, stream=stream)
+            e1.record(stream)
+            nk.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        us = statistics.mean(a.elapsed_time(b) for a, b in nk) * 1e3
+        row_elems = w.new_rows.shape[1]
+        row_out = {0: 1152, 1: 584, 2: 648}[c.layout]
+        nbytes = nr * (row_elems * 2 + row_out + 4 + 4 + 64 * 4) + 512 * 2
+        kvnr = {"rows": nr, "us": us, "alg_bytes": nbytes, "gbps": nbytes / (us * 1e-6) / 1e9,
+                "note": "raw rows -> RMSNorm + RoPE (fp32) -> bf16 -> cache rows; L2 flushed; launch-bound at this size"}
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     value = world * T / (ms_per_step * 1e-3)
@@ -496,6 +524,7 @@ def main():
             "kv_gbps": world * cost["kv_bytes"] / (ms_per_step * 1e-3) / 1e9,
             "kernel_ms": {"kv_write": statistics.mean(kvw_ms), "decode": statistics.mean(dec_ms),
                           "combine": statistics.mean(cmb_ms)},
+            "kv_write_norm_rope": kvnr,
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "steps": args.e2e_steps, "matches_device_path": e2e_matches,

@@ -22,8 +22,8 @@
  *    "host" pointers are ordinary host memory. Nothing is freed or kept.
  *  - Device work is enqueued on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream) and is asynchronous. mla_decode,
- *    mla_combine, mla_kv_write and mla_kv_gather perform no host
- *    synchronisation and no device allocation.
+ *    mla_combine, mla_kv_write, mla_kv_write_norm_rope and mla_kv_gather perform
+ *    no host synchronisation and no device allocation.
  *  - bf16 = IEEE bfloat16 bit patterns (uint16); all row-major, contiguous.
  *
  * KV layouts (one page = page_size rows, page_size a power of two >= 8):
@@ -227,6 +227,33 @@ int mla_combine(const float* part_out, const float* part_lse, const int32_t* num
  */
 int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cache, mla_kv_layout layout,
                  int64_t num_pages, int32_t page_size, void* stream);
+
+/*
+ * Normalise, rotate and write new KV rows (device): the step that produces a
+ * cache row from the latent projection, fused with mla_kv_write ("MLA" API page
+ * of HALOps, mla_attention: "q / kv RMSNorm + RoPE + KV cache write"; its
+ * kv_norm_weight, kv_eps, positions and freqs_real parameters).
+ *  raw     device bf16 [n, row_elems], the un-normalised rows; row_elems = 576
+ *          for layouts 0 and 2 ([kv_c 512 | k_pe 64]) and 512 for layout 1 (the
+ *          DSV4 row: 448 NoPE | 64 RoPE).
+ *  slots   device int32 [n] as for mla_kv_write (negative slots are skipped).
+ *  positions device int32 [n]: the token position that selects the RoPE row;
+ *          rows whose position is outside [0, max_pos) are skipped (not written).
+ *  norm_weight device bf16 [512]: the RMSNorm gain; eps: the RMSNorm epsilon.
+ *  freqs   device float [max_pos, 64]: per position 32 interleaved (cos, sin) pairs.
+ * For every row, in fp32:
+ *  - RMSNorm of the 512 latent elements (elements 0..511):
+ *    y = x * (1 / sqrt(sum(x^2) / 512 + eps)) * w;
+ *  - RoPE of the 64 RoPE elements, pair i = (x[2i], x[2i+1]) of that part, with
+ *    (c, s) = (freqs[pos, 2i], freqs[pos, 2i+1]): (x0 c - x1 s, x0 s + x1 c).
+ *    Layouts 0 and 2 rotate the raw k_pe (elements 512..575, not normalised);
+ *    layout 1 rotates elements 448..511 after the normalisation;
+ *  - the row is rounded to bf16 (nearest even) and written exactly as
+ *    mla_kv_write writes that bf16 row.
+ */
+int mla_kv_write_norm_rope(const void* raw, const int32_t* slots, const int32_t* positions, const void* norm_weight,
+                           float eps, const float* freqs, int32_t max_pos, int32_t n, void* kv_cache,
+                           mla_kv_layout layout, int64_t num_pages, int32_t page_size, void* stream);
 
 /*
  * Page gather (device, a test export): out[j, :] = decoded K row j of one

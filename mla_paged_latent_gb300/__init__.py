@@ -49,7 +49,8 @@ class _PlanInfo(ctypes.Structure):
 
 
 EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_decode_static_workspace", "mla_combine",
-           "mla_kv_write", "mla_kv_gather", "mla_workspace_init", "mla_read_status", "mla_last_error"]
+           "mla_kv_write", "mla_kv_write_norm_rope", "mla_kv_gather", "mla_workspace_init", "mla_read_status",
+           "mla_last_error"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
 
@@ -74,6 +75,7 @@ def load(path: str | None = None):
                                                     V, V, I32, I32, V, V, V, V]
         lib.mla_combine.argtypes = [V, V, V, I32, I32, I32, V, V, V, V]
         lib.mla_kv_write.argtypes = [V, V, I32, V, I32, I64, I32, V]
+        lib.mla_kv_write_norm_rope.argtypes = [V, V, V, V, F32, V, I32, I32, V, I32, I64, I32, V]
         lib.mla_kv_gather.argtypes = [V, I32, I64, I32, V, I32, I32, V, V]
         lib.mla_workspace_init.argtypes = [V, V]
         lib.mla_read_status.argtypes = [V, ctypes.POINTER(ctypes.c_uint32), I32, V]
@@ -211,6 +213,17 @@ def mla_kv_write(rows, slots, kv_cache, layout: int, page_size: int, stream=None
     _require_cuda(rows, slots, kv_cache)
     _check(load().mla_kv_write(_ptr(rows), _ptr(slots), slots.shape[0], _ptr(kv_cache), layout, kv_cache.shape[0],
                                page_size, _stream(stream)))
+
+
+def mla_kv_write_norm_rope(raw, slots, positions, norm_weight, eps: float, freqs, kv_cache, layout: int,
+                           page_size: int, stream=None):
+    """RMSNorm + RoPE + write of new KV rows: raw bf16 [n, 576] (layouts 0, 2) or [n, 512] (layout 1);
+    slots int32 [n]; positions int32 [n]; norm_weight bf16 [512]; freqs float32 [max_pos, 64]
+    (32 interleaved (cos, sin) pairs per position). All on the GPU."""
+    _require_cuda(raw, slots, positions, norm_weight, freqs, kv_cache)
+    _check(load().mla_kv_write_norm_rope(_ptr(raw), _ptr(slots), _ptr(positions), _ptr(norm_weight), float(eps),
+                                         _ptr(freqs), freqs.shape[0], slots.shape[0], _ptr(kv_cache), layout,
+                                         kv_cache.shape[0], page_size, _stream(stream)))
 
 
 def mla_kv_gather(kv_cache, layout: int, page_size: int, block_table_row, length: int, out, stream=None):

@@ -300,6 +300,35 @@ int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cac
   return MLA_OK;
 }
 
+int mla_kv_write_norm_rope(const void* raw, const int32_t* slots, const int32_t* positions, const void* norm_weight,
+                           float eps, const float* freqs, int32_t max_pos, int32_t n, void* kv_cache,
+                           mla_kv_layout layout, int64_t num_pages, int32_t page_size, void* stream) {
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: n < 0");
+  if (n == 0) return MLA_OK;
+  if (!raw || !slots || !positions || !norm_weight || !freqs || !kv_cache)
+    return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: NULL pointer");
+  int64_t rb, pb;
+  int dqk;
+  if (layout_geometry(layout, page_size, &rb, &pb, &dqk) != 0)
+    return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: unknown layout %d", static_cast<int>(layout));
+  if (!pow2(page_size))
+    return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: page_size %d not a power of two", page_size);
+  if (num_pages < 1) return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: num_pages < 1");
+  if (max_pos < 1) return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: max_pos < 1");
+  if (!(eps >= 0.f) || !(eps < 1e30f))
+    return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: eps must be a finite number >= 0");
+  if (!aligned16(raw) || !aligned16(kv_cache) || !aligned16(norm_weight) ||
+      (reinterpret_cast<uintptr_t>(freqs) & 3u) != 0)
+    return fail(MLA_ERR_INVALID_ARG,
+                "mla_kv_write_norm_rope: raw, norm_weight and kv_cache must be 16-byte aligned, freqs 4-byte aligned");
+  cudaError_t e = mla::launch_kv_write_norm_rope(
+      static_cast<const uint16_t*>(raw), slots, positions, static_cast<const uint16_t*>(norm_weight), eps, freqs,
+      max_pos, n, static_cast<uint8_t*>(kv_cache), static_cast<int>(layout), num_pages, page_size, pb,
+      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_kv_write_norm_rope: launch");
+  return MLA_OK;
+}
+
 int mla_kv_gather(const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
                   const int32_t* block_table_row, int32_t max_pages, int32_t length, float* out, void* stream) {
   if (length < 0) return fail(MLA_ERR_INVALID_ARG, "mla_kv_gather: length < 0");

@@ -153,32 +153,19 @@ __device__ __forceinline__ float pow2neg(int e) {
   return __uint_as_float(static_cast<uint32_t>(E) << 23);
 }
 
-// One warp per new row ("MLA" API page of HALOps, mla_attention: KV cache write
-// of the RMSNorm'd row; kv_cache parameter for the layout).
-__global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restrict__ rows,
-                                                       const int32_t* __restrict__ slots, int n,
-                                                       uint8_t* __restrict__ kv, int layout, int64_t num_pages,
-                                                       int page_size, int64_t page_bytes) {
-  pdl_trigger();
-  pdl_wait();
-  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= n) return;
-  const int64_t slot = slots[r];
-  if (slot < 0) return;
-  const int64_t page = slot / page_size;
-  if (page >= num_pages) return;
-  const int off = static_cast<int>(slot % page_size);
+// Write one bf16 row (generic pointer x, 16-byte aligned, row_elems values) into its
+// page slot; all 32 lanes of the warp take part ("MLA" API page of HALOps,
+// mla_attention: KV cache write of the RMSNorm'd row; kv_cache parameter for the layout).
+__device__ __forceinline__ void write_row(const uint16_t* x, int lane, uint8_t* __restrict__ kv, int layout,
+                                          int64_t page, int off, int page_size, int64_t page_bytes) {
   if (layout == 0) {
-    const uint4* src = reinterpret_cast<const uint4*>(rows + (int64_t)r * 576);
+    const uint4* src = reinterpret_cast<const uint4*>(x);
     uint4* dst = reinterpret_cast<uint4*>(kv + page * page_bytes + (int64_t)off * 1152);
     for (int c = lane; c < 72; c += 32) dst[c] = src[c];
     return;
   }
   const int nope = layout == 1 ? 448 : 512;
-  const int row_elems = layout == 1 ? 512 : 576;
   const int row_bytes = layout == 1 ? 576 : 640;
-  const uint16_t* x = rows + (int64_t)r * row_elems;
   uint8_t* dst = kv + page * page_bytes + (int64_t)off * row_bytes;
   uint32_t sbytes[2] = {0u, 0u};
   for (int g = 0; g < nope / 64; ++g) {
@@ -202,6 +189,104 @@ __global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restric
     uint2* sp = reinterpret_cast<uint2*>(kv + page * page_bytes + (int64_t)page_size * row_bytes + off * 8);
     *sp = make_uint2(sbytes[0], sbytes[1]);
   }
+}
+
+// One warp per new row, already normalised.
+__global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restrict__ rows,
+                                                       const int32_t* __restrict__ slots, int n,
+                                                       uint8_t* __restrict__ kv, int layout, int64_t num_pages,
+                                                       int page_size, int64_t page_bytes) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= n) return;
+  const int64_t slot = slots[r];
+  if (slot < 0) return;
+  const int64_t page = slot / page_size;
+  if (page >= num_pages) return;
+  const int row_elems = layout == 1 ? 512 : 576;
+  write_row(rows + (int64_t)r * row_elems, lane, kv, layout, page, static_cast<int>(slot % page_size), page_size,
+            page_bytes);
+}
+
+// One warp per raw row: RMSNorm of the 512 latent elements and RoPE of the 64 RoPE
+// elements in fp32 ("MLA" API page of HALOps, mla_attention: "q / kv RMSNorm + RoPE
+// + KV cache write", kv_norm_weight / kv_eps / positions / freqs_real), the row
+// rounded to bf16 in shared memory, then written as write_row writes it. Lane l
+// holds latent elements [16 l, 16 l + 16) and RoPE pair l of the 576-wide layouts.
+__global__ void __launch_bounds__(128) kv_write_norm_rope_kernel(
+    const uint16_t* __restrict__ raw, const int32_t* __restrict__ slots, const int32_t* __restrict__ positions,
+    const uint16_t* __restrict__ w, float eps, const float* __restrict__ freqs, int max_pos, int n,
+    uint8_t* __restrict__ kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ __align__(16) uint16_t srow[4][576];
+  const int wi = threadIdx.x >> 5;
+  const int r = blockIdx.x * 4 + wi;
+  const int lane = threadIdx.x & 31;
+  if (r >= n) return;
+  const int64_t slot = slots[r];
+  if (slot < 0) return;
+  const int64_t page = slot / page_size;
+  if (page >= num_pages) return;
+  const int pos = positions[r];
+  if (pos < 0 || pos >= max_pos) return;
+  const int row_elems = layout == 1 ? 512 : 576;
+  const uint16_t* x = raw + (int64_t)r * row_elems;
+  const float* f = freqs + (int64_t)pos * 64;
+  float v[16];
+  {
+    const uint4 a = reinterpret_cast<const uint4*>(x)[2 * lane];
+    const uint4 b = reinterpret_cast<const uint4*>(x)[2 * lane + 1];
+    const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = bf16_to_f32(h[k] & 0xFFFFu);
+      v[2 * k + 1] = bf16_to_f32(h[k] >> 16);
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) ss = fmaf(v[k], v[k], ss);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float rinv = 1.0f / sqrtf(ss * (1.0f / 512.0f) + eps);
+  {
+    const uint4 a = reinterpret_cast<const uint4*>(w)[2 * lane];
+    const uint4 b = reinterpret_cast<const uint4*>(w)[2 * lane + 1];
+    const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = v[2 * k] * rinv * bf16_to_f32(h[k] & 0xFFFFu);
+      v[2 * k + 1] = v[2 * k + 1] * rinv * bf16_to_f32(h[k] >> 16);
+    }
+  }
+  if (layout == 1 && lane >= 28) {
+    // DSV4 row: elements 448..511 (lanes 28-31) are the RoPE part, rotated after the norm
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = 8 * (lane - 28) + k;
+      const float c = f[2 * i], s = f[2 * i + 1];
+      const float x0 = v[2 * k], x1 = v[2 * k + 1];
+      v[2 * k] = x0 * c - x1 * s;
+      v[2 * k + 1] = x0 * s + x1 * c;
+    }
+  }
+  uint32_t o[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) o[k] = f32x2_to_bf16x2(v[2 * k], v[2 * k + 1]);
+  reinterpret_cast<uint4*>(srow[wi])[2 * lane] = make_uint4(o[0], o[1], o[2], o[3]);
+  reinterpret_cast<uint4*>(srow[wi])[2 * lane + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  if (layout != 1) {
+    // k_pe (elements 512..575) is rotated as it comes, without the norm
+    const uint32_t two = reinterpret_cast<const uint32_t*>(x + 512)[lane];
+    const float x0 = bf16_to_f32(two & 0xFFFFu), x1 = bf16_to_f32(two >> 16);
+    const float c = f[2 * lane], s = f[2 * lane + 1];
+    reinterpret_cast<uint32_t*>(srow[wi] + 512)[lane] = f32x2_to_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+  }
+  __syncwarp();
+  write_row(srow[wi], lane, kv, layout, page, static_cast<int>(slot % page_size), page_size, page_bytes);
 }
 
 // ----------------------------------------------------------------------------- gather
@@ -259,6 +344,15 @@ cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, u
   if (n <= 0) return cudaSuccess;
   return launch_pdl(kv_write_kernel, dim3((n + 3) / 4), dim3(128), 0, stream, rows, slots, n, kv, layout, num_pages,
                     page_size, page_bytes);
+}
+
+cudaError_t launch_kv_write_norm_rope(const uint16_t* raw, const int32_t* slots, const int32_t* positions,
+                                     const uint16_t* norm_weight, float eps, const float* freqs, int max_pos, int n,
+                                     uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
+                                     cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  return launch_pdl(kv_write_norm_rope_kernel, dim3((n + 3) / 4), dim3(128), 0, stream, raw, slots, positions,
+                    norm_weight, eps, freqs, max_pos, n, kv, layout, num_pages, page_size, page_bytes);
 }
 
 cudaError_t launch_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,

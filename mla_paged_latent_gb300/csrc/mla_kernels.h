@@ -61,6 +61,11 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
 cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout,
                             int64_t num_pages, int page_size, int64_t page_bytes, cudaStream_t stream);
 
+cudaError_t launch_kv_write_norm_rope(const uint16_t* raw, const int32_t* slots, const int32_t* positions,
+                                     const uint16_t* norm_weight, float eps, const float* freqs, int max_pos, int n,
+                                     uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
+                                     cudaStream_t stream);
+
 cudaError_t launch_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
                              const int32_t* bt_row, int max_pages, int length, float* out, cudaStream_t stream);
 

@@ -83,6 +83,10 @@ def _load():
         lib.mo_kv_write.argtypes = [P, P, i32, P, i32, i64, i32]
         lib.mo_kv_write.restype = i32
         lib.mo_kv_gather.argtypes = [P, i32, i64, i32, P, i32, i32, P]
+        lib.mo_bf16_encode.argtypes = [f64]
+        lib.mo_bf16_encode.restype = ctypes.c_uint16
+        lib.mo_kv_norm_rope.argtypes = [P, P, P, f64, P, i32, i32, i32, P]
+        lib.mo_kv_norm_rope.restype = i32
         lib.mo_kv_gather.restype = i32
         _lib = lib
         return lib
@@ -220,6 +224,39 @@ def kv_write(rows_bits, slots, kv_cache: np.ndarray, layout: int, page_size: int
     if rc != 0:
         raise ValueError("oracle: slot out of range")
     return kv
+
+
+def bf16_encode(x) -> np.ndarray:
+    """bfloat16 bits (uint16) of float64 values, rounded once to nearest even."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float64)
+    return np.array([lib.mo_bf16_encode(float(v)) for v in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def kv_norm_rope(raw_bits, positions, weight_bits, eps, freqs, layout: int) -> np.ndarray:
+    """RMSNorm + RoPE of raw KV rows (uint16 bf16 bits [n, row_elems]) -> bf16 bits of the
+    rows mla_kv_write would take. eps is taken at float32 precision (the kernel's);
+    rows with a position outside [0, len(freqs)) come back as zeros."""
+    lib = _load()
+    x = _c(raw_bits, np.uint16)
+    pos = _c(positions, np.int32)
+    w = _c(weight_bits, np.uint16)
+    f = _c(freqs, np.float32)
+    assert w.shape[0] == 512 and f.shape[1] == 64
+    out = np.zeros_like(x)
+    lib.mo_kv_norm_rope(_ptr(x), _ptr(pos), _ptr(w), float(np.float32(eps)), _ptr(f), f.shape[0], x.shape[0], layout,
+                        _ptr(out))
+    return out
+
+
+def kv_write_norm_rope(raw_bits, slots, positions, weight_bits, eps, freqs, kv_cache, layout: int,
+                       page_size: int) -> np.ndarray:
+    """kv_write of kv_norm_rope's rows; a row with an out-of-range position is not written."""
+    rows = kv_norm_rope(raw_bits, positions, weight_bits, eps, freqs, layout)
+    s = np.array(slots, dtype=np.int32, copy=True)
+    p = np.asarray(positions)
+    s[(p < 0) | (p >= np.asarray(freqs).shape[0])] = -1
+    return kv_write(rows, s, kv_cache, layout, page_size)
 
 
 def kv_gather(kv_cache, layout, page_size, block_table_row, length) -> np.ndarray:

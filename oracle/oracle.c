@@ -25,6 +25,9 @@
  *              row size), attn_sink parameter (per-head logit added to the
  *              softmax denominator), and the supported-config paragraph (one
  *              ue8m0 scale per 64 NoPE elements, value dim 512).
+ *              The same entry's kv_norm_weight, kv_eps, positions and freqs_real
+ *              parameters and its "q / kv RMSNorm + RoPE + KV cache write" step
+ *              define mo_kv_norm_rope.
  *  [sglang-FlashMLA] "Implementation:Sgl project Sglang Flash MLA", I/O Contract
  *              (q, k_cache, block_table, cache_seqlens, softmax_scale, causal,
  *              indices -> out, softmax_lse).
@@ -42,6 +45,11 @@
  *    are skipped; duplicates count as often as they appear.
  *  - The fp8 group exponent is the smallest e with 448 * 2^e >= max(amax, 1e-10),
  *    the eps being the fp32 value of 1e-10 (the kernel's precision).
+ *  - RMSNorm covers the 512 latent elements with the mean of squares over 512;
+ *    RoPE pairs are adjacent elements (interleaved), rotated by the table's
+ *    (cos, sin); k_pe of the 576-wide rows is rotated but not normalised; the
+ *    normalised row is rounded to bf16 once and then written as mo_kv_write
+ *    writes a bf16 row.
  */
 #include <math.h>
 #include <stdint.h>
@@ -375,6 +383,74 @@ int mo_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, 
     memcpy(dst + nope, x + nope, 128);
   }
   return 0;
+}
+
+/* bfloat16 encoding of a binary64 value, rounded once to nearest (ties to even)
+ * on the bfloat16 grid (8 significant bits, binary32 exponent range, subnormal
+ * quantum 2^-133); overflow gives infinity. */
+uint16_t mo_bf16_encode(double x) {
+  if (isnan(x)) return 0x7FC0u;
+  const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  const double a = fabs(x);
+  if (a == 0.0) return sign;
+  int k;
+  frexp(a, &k); /* a in [2^(k-1), 2^k) */
+  int eb = k - 1;
+  if (eb < -126) eb = -126;
+  const double quantum = ldexp(1.0, eb - 7);
+  const double y = nearbyint(a / quantum) * quantum;
+  if (y >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);
+  const float fy = (float)y; /* exact: y lies on the bfloat16 grid */
+  uint32_t u;
+  memcpy(&u, &fy, sizeof u);
+  return (uint16_t)((u >> 16) | sign);
+}
+
+/* RMSNorm + RoPE of new KV rows ([HALOps-MLA] mla_attention: the kv RMSNorm +
+ * RoPE before the KV cache write; kv_norm_weight (gain of the 512 latent
+ * elements), kv_eps, positions, and freqs_real: per position 32 interleaved
+ * (cos, sin) pairs). Row i (bf16 bits, row_elems = 576 for layouts 0 and 2,
+ * 512 for layout 1):
+ *   y[d] = x[d] / sqrt(sum_{e<512} x[e]^2 / 512 + eps) * w[d]   for d < 512;
+ *   RoPE pair i of the 64 RoPE elements, (c, s) = freqs[pos, 2i], freqs[pos, 2i+1]:
+ *   (u, v) -> (u c - v s, u s + v c); layouts 0 and 2 rotate the raw elements
+ *   512..575 (k_pe is not normalised), layout 1 rotates y[448..511];
+ * the row is then rounded to bfloat16. Rows whose position lies outside
+ * [0, max_pos) are left as zeros and return a count of them. */
+int mo_kv_norm_rope(const uint16_t* raw, const int32_t* positions, const uint16_t* w, double eps, const float* freqs,
+                    int max_pos, int n, int layout, uint16_t* out) {
+  const int row_elems = layout == 1 ? 512 : 576;
+  int bad = 0;
+  for (int i = 0; i < n; ++i) {
+    const uint16_t* x = raw + (size_t)i * row_elems;
+    uint16_t* o = out + (size_t)i * row_elems;
+    const int pos = positions[i];
+    if (pos < 0 || pos >= max_pos) {
+      memset(o, 0, sizeof(uint16_t) * row_elems);
+      ++bad;
+      continue;
+    }
+    double y[576];
+    double ss = 0.0;
+    for (int d = 0; d < 512; ++d) {
+      const double v = mo_bf16_decode(x[d]);
+      ss += v * v;
+    }
+    const double r = 1.0 / sqrt(ss / 512.0 + eps);
+    for (int d = 0; d < 512; ++d) y[d] = mo_bf16_decode(x[d]) * r * mo_bf16_decode(w[d]);
+    if (layout != 1)
+      for (int d = 512; d < 576; ++d) y[d] = mo_bf16_decode(x[d]);
+    const int rope0 = layout == 1 ? 448 : 512;
+    const float* f = freqs + (size_t)pos * 64;
+    for (int p = 0; p < 32; ++p) {
+      const double c = f[2 * p], sn = f[2 * p + 1];
+      const double u = y[rope0 + 2 * p], v = y[rope0 + 2 * p + 1];
+      y[rope0 + 2 * p] = u * c - v * sn;
+      y[rope0 + 2 * p + 1] = u * sn + v * c;
+    }
+    for (int d = 0; d < row_elems; ++d) o[d] = mo_bf16_encode(y[d]);
+  }
+  return bad;
 }
 
 /* Decoded rows 0..L-1 of one request (block_table row given) -> out [L, dqk]. */

@@ -51,6 +51,70 @@ def test_kv_write_bit_exact(layout):
     assert diff.size == 0, f"{len(diff)} bytes differ, first at {diff[:5].tolist()}"
 
 
+def _rope_table(max_pos):
+    theta = np.outer(np.arange(max_pos), 10000.0 ** (-np.arange(32) / 32.0))
+    f = np.zeros((max_pos, 64), np.float32)
+    f[:, 0::2] = np.cos(theta)
+    f[:, 1::2] = np.sin(theta)
+    return f
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
+def test_kv_write_norm_rope(layout):
+    """RMSNorm + RoPE + write against the oracle. The kernel normalises in fp32 and the
+    oracle in fp64, so a value whose exact result lies within ~1e-6 of a bf16 rounding
+    boundary may round the other way: bytes must agree almost everywhere, and every
+    written value must lie within one step of its output grid of the oracle's."""
+    rng = np.random.default_rng(60 + layout)
+    ps, num_pages, n, max_pos = 16, 12, 150, 4096
+    pb = workloads.page_bytes(layout, ps)
+    re = workloads.row_elems(layout)
+    kv0 = rng.integers(0, 256, (num_pages, pb), dtype=np.uint8)
+    x = (rng.standard_normal((n, re)) * 2.0 ** rng.integers(-20, 20, (n, 1))).astype(np.float32)
+    x[0] = 0.0
+    x[1] = 1e-30
+    x[5, :64] = 0.0
+    raw = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w = torch.from_numpy((1 + 0.2 * rng.standard_normal(512)).astype(np.float32)).to(torch.bfloat16)
+    wbits = w.view(torch.int16).numpy().view(np.uint16)
+    freqs = _rope_table(max_pos)
+    pos = rng.integers(0, max_pos, n).astype(np.int32)
+    pos[2], pos[3] = -1, max_pos
+    slots = rng.permutation(num_pages * ps)[:n].astype(np.int32)
+    slots[4] = -1
+    eps = 1e-6
+    ref = oracle.kv_write_norm_rope(raw, slots, pos, wbits, eps, freqs, kv0, layout, ps)
+    kv = torch.from_numpy(kv0).cuda()
+    mla.mla_kv_write_norm_rope(bf16_tensor(raw), torch.from_numpy(slots).cuda(), torch.from_numpy(pos).cuda(),
+                               bf16_tensor(wbits), eps, torch.from_numpy(freqs).cuda(), kv, layout, ps)
+    got = kv.cpu().numpy()
+    info = oracle.layout_info(layout, ps)
+    rb = info["row_bytes"]
+    written = [(r, int(s)) for r, s in enumerate(slots) if s >= 0 and 0 <= pos[r] < max_pos]
+    mask = np.zeros_like(kv0, dtype=bool)
+    for _, s in written:
+        p, o = divmod(s, ps)
+        mask[p, o * rb:(o + 1) * rb] = True
+        if layout != 0:
+            mask[p, ps * rb + o * 8:ps * rb + o * 8 + 8] = True
+    assert np.array_equal(got[~mask], ref[~mask]), "bytes outside the written rows changed"
+    assert np.array_equal(got[~mask], kv0[~mask])
+    frac = np.mean(got[mask] != ref[mask])
+    assert frac <= 5e-3, f"{frac:.4f} of the written bytes differ from the oracle"
+    nope = info["nope"] if layout != 0 else 0
+    for r, s in written:
+        p, o = divmod(s, ps)
+        g = oracle.decode_row(got, layout, ps, p, o)
+        e = oracle.decode_row(ref, layout, ps, p, o)
+        # bf16 elements: one bf16 step (2^-7 relative); fp8 groups: one e4m3 step (2^-3 relative),
+        # with a floor of 2^-8 of the group's largest magnitude for the subnormal codes
+        tol = np.abs(e) * 2.0 ** -7
+        for gi in range(nope // 64):
+            grp = e[gi * 64:(gi + 1) * 64]
+            tol[gi * 64:(gi + 1) * 64] = np.abs(grp) * 2.0 ** -3 + np.abs(grp).max() * 2.0 ** -8
+        assert np.all(np.abs(g - e) <= tol + 1e-38), f"row {r}: max excess {np.max(np.abs(g - e) - tol):.3g}"
+
+
 @pytest.mark.parametrize("layout", [0, 1, 2])
 def test_kv_gather_bit_exact(layout):
     cfg = workloads.dsv4(batch=2, seqlens=(77, 150), len_dist="fixed", page_size=16, layout=layout)

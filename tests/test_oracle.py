@@ -436,3 +436,131 @@ def test_kv_gather_matches_decode_row(oracle_lib):
     g = oracle.kv_gather(w.kv_cache, 1, 16, w.block_table[1], 70)
     for j in (0, 15, 16, 69):
         assert np.array_equal(g[j], oracle.decode_row(w.kv_cache, 1, 16, w.block_table[1, j // 16], j % 16))
+
+
+# ----------------------------------------------------------------------------- RMSNorm + RoPE (kv write input)
+def _bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_val(bits):
+    return torch.from_numpy(np.asarray(bits).view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+
+
+def _freqs(max_pos, cos, sin):
+    f = np.zeros((max_pos, 64), np.float32)
+    f[:, 0::2] = cos
+    f[:, 1::2] = sin
+    return f
+
+
+def test_bf16_encode_matches_torch_on_fp32_values(oracle_lib):
+    # float32 inputs, so torch's float32 -> bfloat16 rounding (nearest even) is the reference
+    rng = np.random.default_rng(40)
+    x = (rng.standard_normal(4000) * 2.0 ** rng.integers(-60, 60, 4000)).astype(np.float32)
+    assert np.array_equal(oracle.bf16_encode(x.astype(np.float64)), _bf16_bits(x))
+
+
+def test_bf16_encode_ties_subnormals_overflow(oracle_lib):
+    # ties go to the even significand; the subnormal step is 2^-133; overflow is inf
+    cases = [(1 + 2.0 ** -8, 0x3F80), (1 + 3 * 2.0 ** -8, 0x3F82), (-(1 + 2.0 ** -8), 0xBF80), (2.0 ** -133, 0x0001),
+             (2.0 ** -134, 0x0000), (3 * 2.0 ** -134, 0x0002), (2.0 ** 128, 0x7F80), (-0.0, 0x8000), (0.0, 0x0000),
+             (float(np.float32(3.3895314e38)), 0x7F7F)]
+    for v, bits in cases:
+        assert int(oracle.bf16_encode([v])[0]) == bits, (v, hex(int(oracle.bf16_encode([v])[0])))
+
+
+def test_rmsnorm_constant_row_is_unit(oracle_lib):
+    # constant row c with eps = 0 and gain 1: every element becomes sign(c) exactly
+    raw = np.zeros((3, 576), np.float32)
+    raw[0, :512] = 3.5
+    raw[1, :512] = -0.001
+    raw[2, :512] = 1e20
+    out = oracle.kv_norm_rope(_bf16_bits(raw), np.zeros(3, np.int32), _bf16_bits(np.ones(512)), 0.0,
+                              _freqs(1, 1.0, 0.0), 0)
+    assert np.all(_bf16_val(out[0, :512]) == 1.0)
+    assert np.all(_bf16_val(out[1, :512]) == -1.0)
+    assert np.all(_bf16_val(out[2, :512]) == 1.0)
+
+
+def test_rmsnorm_single_spike_closed_form(oracle_lib):
+    # one nonzero latent element a: it becomes sign(a) * sqrt(512), the others stay 0
+    raw = np.zeros((2, 576), np.float32)
+    raw[0, 77] = 5.0
+    raw[1, 500] = -0.25
+    out = oracle.kv_norm_rope(_bf16_bits(raw), np.zeros(2, np.int32), _bf16_bits(np.ones(512)), 0.0,
+                              _freqs(1, 1.0, 0.0), 0)
+    s512 = float(torch.tensor(math.sqrt(512.0), dtype=torch.float64).to(torch.bfloat16).double())
+    assert _bf16_val(out[0, 77]) == s512 and _bf16_val(out[1, 500]) == -s512
+    assert np.count_nonzero(_bf16_val(out[:, :512])) == 2
+
+
+def test_rmsnorm_against_closed_form_and_gain(oracle_lib):
+    # y = x / sqrt(mean(x^2) + eps) * w to within half a bf16 step; a gain of 2 doubles every bit pattern
+    rng = np.random.default_rng(41)
+    x = (rng.standard_normal((6, 576)) * 3).astype(np.float32)
+    w = (1 + 0.1 * rng.standard_normal(512)).astype(np.float32)
+    xb, wb = _bf16_val(_bf16_bits(x)), _bf16_val(_bf16_bits(w))
+    eps = np.float32(0.5)
+    out = oracle.kv_norm_rope(_bf16_bits(x), np.zeros(6, np.int32), _bf16_bits(w), eps, _freqs(1, 1.0, 0.0), 0)
+    ref = xb[:, :512] / np.sqrt((xb[:, :512] ** 2).mean(1, keepdims=True) + float(eps)) * wb
+    got = _bf16_val(out[:, :512])
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+    out2 = oracle.kv_norm_rope(_bf16_bits(x), np.zeros(6, np.int32), _bf16_bits(2 * wb), eps, _freqs(1, 1.0, 0.0), 0)
+    assert np.array_equal(_bf16_val(out2[:, :512]), 2 * got)
+    # k_pe is not normalised: the identity rotation leaves its bits unchanged
+    assert np.array_equal(out[:, 512:], _bf16_bits(x)[:, 512:])
+
+
+def test_rope_quarter_and_half_turns(oracle_lib):
+    # (u, v) -> (-v, u) for (cos, sin) = (0, 1) and -> (-u, -v) for (-1, 0), exactly, on k_pe
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((4, 576)).astype(np.float32)
+    xb = _bf16_val(_bf16_bits(x))
+    f = np.concatenate([_freqs(1, 0.0, 1.0), _freqs(1, -1.0, 0.0)])
+    out = oracle.kv_norm_rope(_bf16_bits(x), np.array([0, 0, 1, 1], np.int32), _bf16_bits(np.ones(512)), 1e-6, f, 2)
+    pe, got = xb[:, 512:], _bf16_val(out[:, 512:])
+    assert np.array_equal(got[:2, 0::2], -pe[:2, 1::2]) and np.array_equal(got[:2, 1::2], pe[:2, 0::2])
+    assert np.array_equal(got[2:], -pe[2:])
+
+
+def test_rope_matches_complex_rotation(oracle_lib):
+    # interleaved pairs as complex numbers times e^(i theta) (torch complex128), per position
+    rng = np.random.default_rng(43)
+    max_pos = 50
+    theta = np.outer(np.arange(max_pos), 10000.0 ** (-np.arange(32) / 32.0))
+    f = _freqs(max_pos, np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32))
+    x = (rng.standard_normal((7, 576)) * 4).astype(np.float32)
+    pos = np.array([0, 1, 7, 13, 29, 48, 49], np.int32)
+    out = oracle.kv_norm_rope(_bf16_bits(x), pos, _bf16_bits(np.ones(512)), 1e-6, f, 2)
+    pe = torch.from_numpy(_bf16_val(_bf16_bits(x))[:, 512:].reshape(7, 32, 2).copy())
+    rot = torch.complex(torch.from_numpy(f[pos, 0::2].astype(np.float64)), torch.from_numpy(f[pos, 1::2].astype(np.float64)))
+    ref = torch.view_as_real(torch.view_as_complex(pe) * rot).reshape(7, 64).numpy()
+    got = _bf16_val(out[:, 512:])
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 2.0 ** -133)
+
+
+def test_dsv4_row_rotates_after_the_norm(oracle_lib):
+    # layout 1: the 512-wide row is normalised as a whole, then elements 448..511 are rotated
+    rng = np.random.default_rng(44)
+    x = rng.standard_normal((3, 512)).astype(np.float32)
+    w = _bf16_bits(np.ones(512))
+    plain = oracle.kv_norm_rope(_bf16_bits(x), np.zeros(3, np.int32), w, 1e-6, _freqs(1, 1.0, 0.0), 1)
+    quarter = oracle.kv_norm_rope(_bf16_bits(x), np.zeros(3, np.int32), w, 1e-6, _freqs(1, 0.0, 1.0), 1)
+    assert np.array_equal(plain[:, :448], quarter[:, :448])
+    n = _bf16_val(plain[:, 448:])
+    q = _bf16_val(quarter[:, 448:])
+    assert np.array_equal(q[:, 0::2], -n[:, 1::2]) and np.array_equal(q[:, 1::2], n[:, 0::2])
+    ms = (_bf16_val(plain) ** 2).mean(1)
+    assert np.all(np.abs(ms - 1) < 2.0 ** -7)
+
+
+def test_norm_rope_write_skips_bad_positions(oracle_lib):
+    # a row whose position is outside the table is not written
+    rng = np.random.default_rng(45)
+    x = _bf16_bits(rng.standard_normal((3, 576)))
+    kv = rng.integers(0, 256, (1, 16 * 1152), dtype=np.uint8)
+    out = oracle.kv_write_norm_rope(x, np.array([0, 1, 2], np.int32), np.array([0, 5, -1], np.int32),
+                                    _bf16_bits(np.ones(512)), 1e-6, _freqs(4, 1.0, 0.0), kv, 0, 16)
+    assert np.array_equal(out[0, 1152:3 * 1152], kv[0, 1152:3 * 1152])
+    assert not np.array_equal(out[0, :1152], kv[0, :1152])
