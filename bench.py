@@ -351,6 +351,68 @@ def main():
     kvw_ms = [e[0].elapsed_time(e[1]) for e in bd]
     cmb_ms = [e[2].elapsed_time(e[3]) for e in bd]
 
+    # The step after the decode for the 576-wide (DSV3-style) layouts: split combine fused with
+    # the value up-projection o_v = x W_UV[n] (random bf16 W_UV [N, 512, 128]), timed alone on
+    # this step's partials and decode output.
+    cvu = None
+    if c.layout != 1:
+        gen = torch.Generator(device=dev).manual_seed(0)
+        w_uv = (torch.randn(N, 512, 128, device=dev, generator=gen) * 0.05).to(torch.bfloat16)
+        o_v = torch.empty(T, N, 128, dtype=torch.bfloat16, device=dev)
+        out_keep = out.clone()
+        lse_keep = lse.clone()
+        ck = []
+        for k in range(nbd):
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            mla.mla_combine_v_up(part_out if split else None, part_lse if split else None, ns, c.sq, N, w_uv, out, lse,
+                                 o_v, sink=sink, stream=stream)
+            e1.record(stream)
+            ck.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        us = statistics.mean(a.elapsed_time(b) for a, b in ck) * 1e3
+        nsplit_rows = int((np.diff(plan.num_splits) >= 2).astype(np.int64) @ np.full(c.batch, c.sq * N))
+        part_bytes = (plan.total_splits * c.sq * N * (512 * 4 + 4)) if split else 0
+        nbytes = N * 512 * 128 * 2 + part_bytes + T * N * 512 * 2 + nsplit_rows * (512 * 2 + 4) + T * N * 128 * 2
+        flops = 2.0 * T * N * 512 * 128
+        cvu = {"us": us, "alg_bytes": nbytes, "gbps": nbytes / (us * 1e-6) / 1e9, "tflops": flops / (us * 1e-6) / 1e12,
+               "note": "merge of split rows + bf16 latent x W_UV[n] (dv 128) as tcgen05 MMAs, one CTA per head; "
+                       "W_UV random bf16; L2 flushed"}
+        out.copy_(out_keep)   # the merged rows it rewrote; the e2e check compares against the decode's own
+        lse.copy_(lse_keep)
+
+    # The step after the decode for the DSV4 row (value = 448 NoPE + 64 RoPE): split combine fused
+    # with the inverse RoPE of elements 448..511, timed alone on this step's partials and output.
+    cir = None
+    if c.layout == 1:
+        tpos = np.concatenate([np.arange(int(L) - c.sq, int(L)) for L in w.seqlens]).astype(np.int32)
+        max_pos = int(w.seqlens.max()) + 1
+        theta = np.outer(np.arange(max_pos), 10000.0 ** (-np.arange(32) / 32.0))
+        ftab = np.zeros((max_pos, 64), np.float32)
+        ftab[:, 0::2], ftab[:, 1::2] = np.cos(theta), np.sin(theta)
+        d_tpos, d_ftab = torch.from_numpy(tpos).to(dev), torch.from_numpy(ftab).to(dev)
+        out_keep, lse_keep = out.clone(), lse.clone()
+        ck = []
+        for k in range(nbd):
+            out.copy_(out_keep)
+            flush.fill_(k & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            mla.mla_combine_inv_rope(part_out if split else None, part_lse if split else None, ns, c.sq, N, d_tpos,
+                                     d_ftab, out, lse, rope0=448, sink=sink, stream=stream)
+            e1.record(stream)
+            ck.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        out.copy_(out_keep)
+        lse.copy_(lse_keep)
+        us = statistics.mean(a.elapsed_time(b) for a, b in ck) * 1e3
+        nsplit_rows = int((np.diff(plan.num_splits) >= 2).astype(np.int64) @ np.full(c.batch, c.sq * N))
+        part_bytes = (plan.total_splits * c.sq * N * (512 * 4 + 4)) if split else 0
+        nbytes = part_bytes + (T * N - nsplit_rows) * 1024 + T * N * 1024 + nsplit_rows * 4 + T * 4
+        cir = {"us": us, "alg_bytes": nbytes, "gbps": nbytes / (us * 1e-6) / 1e9,
+               "note": "merge of split rows + inverse RoPE of elements 448..511 of every row, in place; L2 flushed"}
+
     # The fused RMSNorm + RoPE + write of the same new rows (raw rows in, cache rows out), timed
     # alone. It rewrites those slots; the e2e loop below writes them back with mla_kv_write.
     kvnr = None
@@ -525,6 +587,8 @@ def main():
             "kernel_ms": {"kv_write": statistics.mean(kvw_ms), "decode": statistics.mean(dec_ms),
                           "combine": statistics.mean(cmb_ms)},
             "kv_write_norm_rope": kvnr,
+            "combine_v_up": cvu,
+            "combine_inv_rope": cir,
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "steps": args.e2e_steps, "matches_device_path": e2e_matches,

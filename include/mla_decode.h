@@ -22,8 +22,9 @@
  *    "host" pointers are ordinary host memory. Nothing is freed or kept.
  *  - Device work is enqueued on `stream` (a cudaStream_t passed as void*;
  *    NULL = the legacy default stream) and is asynchronous. mla_decode,
- *    mla_combine, mla_kv_write, mla_kv_write_norm_rope and mla_kv_gather perform
- *    no host synchronisation and no device allocation.
+ *    mla_combine, mla_combine_v_up, mla_combine_inv_rope, mla_kv_write,
+ *    mla_kv_write_norm_rope and mla_kv_gather perform no host synchronisation and
+ *    no device allocation.
  *  - bf16 = IEEE bfloat16 bit patterns (uint16); all row-major, contiguous.
  *
  * KV layouts (one page = page_size rows, page_size a power of two >= 8):
@@ -213,6 +214,45 @@ int mla_decode_static_workspace(const void* q, const void* kv_cache, mla_kv_layo
  */
 int mla_combine(const float* part_out, const float* part_lse, const int32_t* num_splits, int32_t batch,
                 int32_t rows_per_req, int32_t num_heads, const float* sink, void* out, float* lse, void* stream);
+
+/*
+ * Split combine fused with the value up-projection (device): the step after the
+ * decode in the absorbed form. Every query row's latent output x (512 wide) is
+ * mapped to its head's value space, o_v = x W_UV[n] ("mla_attention.py ·
+ * tduncan/Nvidia-Optimization-Stack-VLLM": _v_up_proj multiplies the (N, B, L)
+ * latent output by W_UV (N, L, V)).
+ *  part_out, part_lse, num_splits, sink: as for mla_combine (part_out and part_lse
+ *         may be NULL when no request has two or more splits).
+ *  w_uv   device bf16 [num_heads, 512, 128] (value head dim 128), 16-byte aligned.
+ *  out    device bf16 [T, N, 512]: read for requests with one split (the decode
+ *         wrote it); for split requests the merged row is written here first,
+ *         exactly as mla_combine writes it (and lse with it).
+ *  o_v    device bf16 [T, N, 128]: o_v[t, n, :] = bf16(sum_l x[t, n, l] W_UV[n, l, :]),
+ *         x being the bf16 latent row, products summed in fp32.
+ *  status optional device uint32 (NULL or a workspace): bit 0 is set when a
+ *         bounded wait ran out (the call then leaves o_v incomplete).
+ */
+int mla_combine_v_up(const float* part_out, const float* part_lse, const int32_t* num_splits, int32_t batch,
+                     int32_t q_tokens_per_req, int32_t num_heads, const float* sink, const void* w_uv, void* out,
+                     float* lse, void* o_v, uint32_t* status, void* stream);
+
+/*
+ * Split combine fused with the inverse RoPE of the output (device): the step after
+ * the decode for rows whose value part carries RoPE (the DSV4 row: value dim 512 =
+ * 448 NoPE + 64 RoPE, O "before the inverse RoPE"; "MLA" API page of HALOps,
+ * mla_output_proj: "the split-KV LSE combine and inverse RoPE of O").
+ * Every row of out [T, N, 512] (bf16, in place) is first merged as mla_combine
+ * merges it when its request has two or more splits (writing lse too), or taken as
+ * the decode wrote it; then elements [rope0, rope0 + 64) are rotated back: pair i =
+ * (u, v) -> (u c + v s, v c - u s) with (c, s) = freqs[positions[t], 2i .. 2i + 1],
+ * in fp32, and rounded to bf16. Rows of a token whose position is outside
+ * [0, max_pos) are merged but not rotated.
+ *  positions device int32 [T]; freqs device float [max_pos, 64]; rope0 a multiple
+ *  of 4 with rope0 + 64 <= 512 (448 for the DSV4 row).
+ */
+int mla_combine_inv_rope(const float* part_out, const float* part_lse, const int32_t* num_splits, int32_t batch,
+                         int32_t q_tokens_per_req, int32_t num_heads, const float* sink, const int32_t* positions,
+                         const float* freqs, int32_t max_pos, int32_t rope0, void* out, float* lse, void* stream);
 
 /*
  * KV-row write (device): scatter n new rows into their pages ("MLA" API page of

@@ -49,7 +49,7 @@ class _PlanInfo(ctypes.Structure):
 
 
 EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_decode_static_workspace", "mla_combine",
-           "mla_kv_write", "mla_kv_write_norm_rope", "mla_kv_gather", "mla_workspace_init", "mla_read_status",
+           "mla_combine_v_up", "mla_combine_inv_rope", "mla_kv_write", "mla_kv_write_norm_rope", "mla_kv_gather", "mla_workspace_init", "mla_read_status",
            "mla_last_error"]
 STATIC_WORKSPACE_BYTES = 64 << 20
 
@@ -74,6 +74,8 @@ def load(path: str | None = None):
         lib.mla_decode_static_workspace.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32,
                                                     V, V, I32, I32, V, V, V, V]
         lib.mla_combine.argtypes = [V, V, V, I32, I32, I32, V, V, V, V]
+        lib.mla_combine_v_up.argtypes = [V, V, V, I32, I32, I32, V, V, V, V, V, V, V]
+        lib.mla_combine_inv_rope.argtypes = [V, V, V, I32, I32, I32, V, V, V, I32, I32, V, V, V]
         lib.mla_kv_write.argtypes = [V, V, I32, V, I32, I64, I32, V]
         lib.mla_kv_write_norm_rope.argtypes = [V, V, V, V, F32, V, I32, I32, V, I32, I64, I32, V]
         lib.mla_kv_gather.argtypes = [V, I32, I64, I32, V, I32, I32, V, V]
@@ -213,6 +215,30 @@ def mla_kv_write(rows, slots, kv_cache, layout: int, page_size: int, stream=None
     _require_cuda(rows, slots, kv_cache)
     _check(load().mla_kv_write(_ptr(rows), _ptr(slots), slots.shape[0], _ptr(kv_cache), layout, kv_cache.shape[0],
                                page_size, _stream(stream)))
+
+
+def mla_combine_v_up(part_out, part_lse, num_splits, q_tokens_per_req: int, num_heads: int, w_uv, out, lse, o_v,
+                     sink=None, status=None, stream=None):
+    """Split combine + value up-projection: o_v [T, N, 128] bf16 = bf16 latent out [T, N, 512] x W_UV[n]
+    (w_uv bf16 [N, 512, 128]); split requests are merged into out / lse first. part_out / part_lse may be
+    None when no request is split. status: optional device uint32 [1] (bit 0: a bounded wait ran out)."""
+    _require_cuda(part_out, part_lse, num_splits, w_uv, out, lse, o_v, sink, status)
+    B = num_splits.shape[0] - 1
+    _check(load().mla_combine_v_up(_ptr(part_out), _ptr(part_lse), _ptr(num_splits), B, q_tokens_per_req, num_heads,
+                                   _ptr(sink), _ptr(w_uv), _ptr(out), _ptr(lse), _ptr(o_v), _ptr(status),
+                                   _stream(stream)))
+
+
+def mla_combine_inv_rope(part_out, part_lse, num_splits, q_tokens_per_req: int, num_heads: int, positions, freqs,
+                         out, lse, rope0: int = 448, sink=None, stream=None):
+    """Split combine + inverse RoPE of out[..., rope0:rope0 + 64] (in place, bf16 [T, N, 512]);
+    positions int32 [T]; freqs float32 [max_pos, 64]. part_out / part_lse may be None when no
+    request is split."""
+    _require_cuda(part_out, part_lse, num_splits, positions, freqs, out, lse, sink)
+    B = num_splits.shape[0] - 1
+    _check(load().mla_combine_inv_rope(_ptr(part_out), _ptr(part_lse), _ptr(num_splits), B, q_tokens_per_req,
+                                       num_heads, _ptr(sink), _ptr(positions), _ptr(freqs), freqs.shape[0], rope0,
+                                       _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def mla_kv_write_norm_rope(raw, slots, positions, norm_weight, eps: float, freqs, kv_cache, layout: int,

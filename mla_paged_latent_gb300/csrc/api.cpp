@@ -300,6 +300,64 @@ int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cac
   return MLA_OK;
 }
 
+int mla_combine_inv_rope(const float* part_out, const float* part_lse, const int32_t* num_splits, int32_t batch,
+                         int32_t q_tokens_per_req, int32_t num_heads, const float* sink, const int32_t* positions,
+                         const float* freqs, int32_t max_pos, int32_t rope0, void* out, float* lse, void* stream) {
+  if (!num_splits || !positions || !freqs || !out || !lse)
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_inv_rope: NULL pointer argument");
+  if (batch < 1 || q_tokens_per_req < 1 || num_heads < 1 || max_pos < 1)
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_inv_rope: batch, q_tokens_per_req, num_heads, max_pos must be >= 1");
+  if (static_cast<int64_t>(batch) * q_tokens_per_req * num_heads >= (1ll << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "mla_combine_inv_rope: too many query rows");
+  if (rope0 < 0 || rope0 % 4 != 0 || rope0 + 64 > 512)
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_inv_rope: rope0 = %d must be a multiple of 4 with rope0 + 64 <= 512",
+                rope0);
+  if ((part_out == nullptr) != (part_lse == nullptr))
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_inv_rope: part_out and part_lse must be given together");
+  if (!aligned16(out) || (part_out && !aligned16(part_out)) || (reinterpret_cast<uintptr_t>(freqs) & 3u))
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_inv_rope: out and part_out must be 16-byte aligned");
+  cudaError_t e = mla::launch_combine_inv_rope(part_out, part_lse, num_splits, batch, q_tokens_per_req, num_heads,
+                                               sink, positions, freqs, max_pos, rope0, static_cast<uint16_t*>(out), lse,
+                                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_combine_inv_rope: launch");
+  return MLA_OK;
+}
+
+int mla_combine_v_up(const float* part_out, const float* part_lse, const int32_t* num_splits, int32_t batch,
+                     int32_t q_tokens_per_req, int32_t num_heads, const float* sink, const void* w_uv, void* out,
+                     float* lse, void* o_v, uint32_t* status, void* stream) {
+  if (!num_splits || !w_uv || !out || !lse || !o_v)
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_v_up: NULL pointer argument");
+  if (batch < 1 || q_tokens_per_req < 1 || num_heads < 1)
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_v_up: batch, q_tokens_per_req and num_heads must be >= 1");
+  if (static_cast<int64_t>(batch) * q_tokens_per_req * num_heads >= (1ll << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "mla_combine_v_up: too many query rows");
+  if ((part_out == nullptr) != (part_lse == nullptr))
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_v_up: part_out and part_lse must be given together");
+  if (!aligned16(w_uv) || !aligned16(out) || !aligned16(o_v) || (part_out && !aligned16(part_out)))
+    return fail(MLA_ERR_INVALID_ARG, "mla_combine_v_up: w_uv, out, o_v and part_out must be 16-byte aligned");
+  int enc_err = 0;
+  EncodeTiledFn encode = get_encode_fn(&enc_err);
+  if (enc_err) return fail(MLA_ERR_CUDA, "mla_combine_v_up: cuTensorMapEncodeTiled is unavailable");
+  CUtensorMap w_map;
+  std::memset(&w_map, 0, sizeof w_map);
+  {
+    const cuuint64_t dims[3] = {128, 512, static_cast<cuuint64_t>(num_heads)};
+    const cuuint64_t strides[2] = {128 * 2, 512 * 128 * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = encode(&w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w_uv), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_combine_v_up: encoding the W_UV tensor map failed (%d)", (int)r);
+  }
+  cudaError_t e = mla::launch_combine_v_up(part_out, part_lse, num_splits, batch, q_tokens_per_req, num_heads, sink,
+                                           static_cast<uint16_t*>(out), lse, static_cast<uint16_t*>(o_v), status,
+                                           w_map, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_combine_v_up: launch");
+  return MLA_OK;
+}
+
 int mla_kv_write_norm_rope(const void* raw, const int32_t* slots, const int32_t* positions, const void* norm_weight,
                            float eps, const float* freqs, int32_t max_pos, int32_t n, void* kv_cache,
                            mla_kv_layout layout, int64_t num_pages, int32_t page_size, void* stream) {

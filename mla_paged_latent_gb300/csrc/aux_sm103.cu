@@ -2,6 +2,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "combine_row.cuh"
 #include "mla_kernels.h"
 #include "ptx_sm103.cuh"
 
@@ -14,12 +15,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float x) {
 __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
 // ----------------------------------------------------------------------------- combine
-// One warp per query row of a request that the plan split into >= 2 pieces:
-// lse = ln sum_s e^(lse_s); out = sum_s e^(lse_s - lse) o_s ("mla_attention.py ·
-// tduncan/Nvidia-Optimization-Stack-VLLM", Chunked Prefill: merge_attn_states;
-// an empty partial has lse = -inf and weight 0); then the sink factor
-// 1 / (1 + e^(sink - lse)) ("MLA" API page of HALOps, mla_output_proj: the
-// split-KV LSE combine receives attn_sink).
+// One warp per query row of a request that the plan split into >= 2 pieces (the merge
+// itself is merge_row in combine_row.cuh).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
                                                       const float* __restrict__ part_lse,
                                                       const int32_t* __restrict__ num_splits, int R, int heads,
@@ -35,97 +32,63 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (row >= R) return;
   const int lane = threadIdx.x & 31;
   const int64_t orow = (int64_t)b * R + row;
-  if (ns <= 4) {
-    // up to 4 splits (the common case): every load first, in one round trip to memory
-    float ls[4];
-    float4 v[4][4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      ls[s] = -INFINITY;
-      if (s < ns) {
-        ls[s] = part_lse[(int64_t)(s0 + s) * R + row];
-        const float4* src = reinterpret_cast<const float4*>(part_out + ((int64_t)(s0 + s) * R + row) * 512);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[s][k] = src[k * 32 + lane];
-      }
-    }
-    const float mx = fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3]));
-    if (mx == -INFINITY) {
-      for (int d = lane; d < 512; d += 32) out[orow * 512 + d] = 0;
-      if (lane == 0) lse[orow] = -INFINITY;
-      return;
-    }
-    float tot = 0.f;
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-      if (s < ns) tot += expf(ls[s] - mx);
-    const float lse_tot = mx + logf(tot);
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      if (s >= ns || ls[s] == -INFINITY) continue;
-      const float w = expf(ls[s] - lse_tot);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[4 * k + 0] += w * v[s][k].x;
-        acc[4 * k + 1] += w * v[s][k].y;
-        acc[4 * k + 2] += w * v[s][k].z;
-        acc[4 * k + 3] += w * v[s][k].w;
-      }
-    }
-    float f = 1.f;
-    if (sink != nullptr) f = 1.f / (1.f + expf(sink[row % heads] - lse_tot));
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t lo = f32x2_to_bf16x2(acc[4 * k] * f, acc[4 * k + 1] * f);
-      const uint32_t hi = f32x2_to_bf16x2(acc[4 * k + 2] * f, acc[4 * k + 3] * f);
-      *reinterpret_cast<uint2*>(out + orow * 512 + (k * 32 + lane) * 4) = make_uint2(lo, hi);
-    }
-    if (lane == 0) lse[orow] = lse_tot;
-    return;
-  }
-  float mx = -INFINITY;
-  for (int s = lane; s < ns; s += 32) mx = fmaxf(mx, part_lse[(int64_t)(s0 + s) * R + row]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (mx == -INFINITY) {
-    for (int d = lane; d < 512; d += 32) out[orow * 512 + d] = 0;
-    if (lane == 0) lse[orow] = -INFINITY;
-    return;
-  }
-  float tot = 0.f;
-  for (int s = lane; s < ns; s += 32) tot += expf(part_lse[(int64_t)(s0 + s) * R + row] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  const float lse_tot = mx + logf(tot);
   float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float ls = part_lse[(int64_t)(s0 + s) * R + row];
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - lse_tot);
-    const float4* src = reinterpret_cast<const float4*>(part_out + ((int64_t)(s0 + s) * R + row) * 512);
+  const float lse_tot = merge_row(part_out, part_lse, s0, ns, R, row, lane, sink, row % heads, acc);
+  store_row_bf16(out + orow * 512, lane, acc);
+  if (lane == 0) lse[orow] = lse_tot;
+}
+
+// One warp per query row: the merged (split) or decode-written (unsplit) row, with the
+// inverse RoPE applied to elements [rope0, rope0 + 64): pair i = (u, v) -> (u c + v s,
+// v c - u s), (c, s) = freqs[pos, 2i], freqs[pos, 2i + 1] ("MLA" API page of HALOps,
+// mla_output_proj: "the split-KV LSE combine and inverse RoPE of O"). Written back to out.
+__global__ void __launch_bounds__(256) combine_inv_rope_kernel(
+    const float* __restrict__ part_out, const float* __restrict__ part_lse, const int32_t* __restrict__ num_splits,
+    int R, int sq, int heads, const float* __restrict__ sink, const int32_t* __restrict__ positions,
+    const float* __restrict__ freqs, int max_pos, int rope0, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= R) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t orow = (int64_t)b * R + row;
+  const int s0 = num_splits[b];
+  const int ns = num_splits[b + 1] - s0;
+  float acc[16];
+  if (ns >= 2) {
+    const float lse_tot = merge_row(part_out, part_lse, s0, ns, R, row, lane, sink, row % heads, acc);
+    store_row_bf16(out + orow * 512, lane, acc);  // acc now holds the bf16 values
+    if (lane == 0) lse[orow] = lse_tot;
+  } else {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float4 v = src[k * 32 + lane];
-      acc[4 * k + 0] += w * v.x;
-      acc[4 * k + 1] += w * v.y;
-      acc[4 * k + 2] += w * v.z;
-      acc[4 * k + 3] += w * v.w;
+      const uint2 v = *reinterpret_cast<const uint2*>(out + orow * 512 + (k * 32 + lane) * 4);
+      acc[4 * k] = __uint_as_float(v.x << 16);
+      acc[4 * k + 1] = __uint_as_float(v.x & 0xFFFF0000u);
+      acc[4 * k + 2] = __uint_as_float(v.y << 16);
+      acc[4 * k + 3] = __uint_as_float(v.y & 0xFFFF0000u);
     }
   }
-  float f = 1.f;
-  if (sink != nullptr) f = 1.f / (1.f + expf(sink[row % heads] - lse_tot));
+  const int pos = positions[b * sq + row / heads];
+  if (pos < 0 || pos >= max_pos) return;  // no table row: left as merged
+  const float* f = freqs + (int64_t)pos * 64;
+  // lane holds elements d = 4 (32 k + lane) .. +3, i.e. pairs (d, d + 1) and (d + 2, d + 3)
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t lo = f32x2_to_bf16x2(acc[4 * k] * f, acc[4 * k + 1] * f);
-    const uint32_t hi = f32x2_to_bf16x2(acc[4 * k + 2] * f, acc[4 * k + 3] * f);
-    *reinterpret_cast<uint2*>(out + orow * 512 + (k * 32 + lane) * 4) = make_uint2(lo, hi);
+    const int d = (k * 32 + lane) * 4;
+    if (d < rope0 || d >= rope0 + 64) continue;
+    const int i = (d - rope0) >> 1;
+    float y[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float c = f[2 * (i + h)], sn = f[2 * (i + h) + 1];
+      const float u = acc[4 * k + 2 * h], v = acc[4 * k + 2 * h + 1];
+      y[2 * h] = u * c + v * sn;
+      y[2 * h + 1] = v * c - u * sn;
+    }
+    *reinterpret_cast<uint2*>(out + orow * 512 + d) = make_uint2(f32x2_to_bf16x2(y[0], y[1]), f32x2_to_bf16x2(y[2], y[3]));
   }
-  if (lane == 0) lse[orow] = lse_tot;
 }
 
 // ----------------------------------------------------------------------------- kv write
@@ -337,6 +300,15 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
   dim3 grid((rows_per_req + 7) / 8, batch);
   return launch_pdl(combine_kernel, grid, dim3(256), 0, stream, part_out, part_lse, num_splits, rows_per_req, heads,
                     sink, out, lse);
+}
+
+cudaError_t launch_combine_inv_rope(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
+                                    int sq, int heads, const float* sink, const int32_t* positions, const float* freqs,
+                                    int max_pos, int rope0, uint16_t* out, float* lse, cudaStream_t stream) {
+  const int R = sq * heads;
+  dim3 grid((R + 7) / 8, batch);
+  return launch_pdl(combine_inv_rope_kernel, grid, dim3(256), 0, stream, part_out, part_lse, num_splits, R, sq, heads,
+                    sink, positions, freqs, max_pos, rope0, out, lse);
 }
 
 cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout,

@@ -66,6 +66,14 @@ cudaError_t launch_kv_write_norm_rope(const uint16_t* raw, const int32_t* slots,
                                      uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
                                      cudaStream_t stream);
 
+cudaError_t launch_combine_inv_rope(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
+                                    int sq, int heads, const float* sink, const int32_t* positions, const float* freqs,
+                                    int max_pos, int rope0, uint16_t* out, float* lse, cudaStream_t stream);
+
+cudaError_t launch_combine_v_up(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
+                                int sq, int heads, const float* sink, uint16_t* out, float* lse, uint16_t* o_v,
+                                unsigned int* status, const CUtensorMap& w_map, cudaStream_t stream);
+
 cudaError_t launch_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
                              const int32_t* bt_row, int max_pages, int length, float* out, cudaStream_t stream);
 

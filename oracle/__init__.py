@@ -83,11 +83,15 @@ def _load():
         lib.mo_kv_write.argtypes = [P, P, i32, P, i32, i64, i32]
         lib.mo_kv_write.restype = i32
         lib.mo_kv_gather.argtypes = [P, i32, i64, i32, P, i32, i32, P]
+        lib.mo_kv_gather.restype = i32
         lib.mo_bf16_encode.argtypes = [f64]
         lib.mo_bf16_encode.restype = ctypes.c_uint16
         lib.mo_kv_norm_rope.argtypes = [P, P, P, f64, P, i32, i32, i32, P]
         lib.mo_kv_norm_rope.restype = i32
-        lib.mo_kv_gather.restype = i32
+        lib.mo_v_up.argtypes = [P, P, i32, i32, i32, P]
+        lib.mo_v_up.restype = None
+        lib.mo_inv_rope.argtypes = [P, P, P, i32, i32, i32, P]
+        lib.mo_inv_rope.restype = None
         _lib = lib
         return lib
 
@@ -257,6 +261,31 @@ def kv_write_norm_rope(raw_bits, slots, positions, weight_bits, eps, freqs, kv_c
     p = np.asarray(positions)
     s[(p < 0) | (p >= np.asarray(freqs).shape[0])] = -1
     return kv_write(rows, s, kv_cache, layout, page_size)
+
+
+def v_up(x_bits, w_bits) -> np.ndarray:
+    """Value up-projection: x bf16 bits [T, N, 512], w bf16 bits [N, 512, dv] -> bf16 bits [T, N, dv]."""
+    lib = _load()
+    x = _c(x_bits, np.uint16)
+    w = _c(w_bits, np.uint16)
+    T, N = x.shape[0], x.shape[1]
+    dv = w.shape[2]
+    assert x.shape[2] == 512 and w.shape[0] == N and w.shape[1] == 512
+    o = np.zeros((T, N, dv), np.uint16)
+    lib.mo_v_up(_ptr(x), _ptr(w), T, N, dv, _ptr(o))
+    return o
+
+
+def inv_rope(x_bits, positions, freqs, rope0: int = 448) -> np.ndarray:
+    """Inverse RoPE of bf16 rows [rows, 512] (elements rope0 .. rope0 + 63), one position per row."""
+    lib = _load()
+    x = _c(x_bits, np.uint16).reshape(-1, 512)
+    pos = _c(positions, np.int32)
+    f = _c(freqs, np.float32)
+    assert pos.shape[0] == x.shape[0] and f.shape[1] == 64
+    out = np.zeros_like(x)
+    lib.mo_inv_rope(_ptr(x), _ptr(pos), _ptr(f), f.shape[0], rope0, x.shape[0], _ptr(out))
+    return out
 
 
 def kv_gather(kv_cache, layout, page_size, block_table_row, length) -> np.ndarray:

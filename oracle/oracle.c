@@ -453,6 +453,43 @@ int mo_kv_norm_rope(const uint16_t* raw, const int32_t* positions, const uint16_
   return bad;
 }
 
+/* Value up-projection ([vLLM-MLA] _v_up_proj: the (N, B, L) latent output times
+ * W_UV (N, L, V)): o[t, n, v] = bf16(sum_l x[t, n, l] * w[n, l, v]) for x the
+ * bf16 latent rows [T, N, 512] and w bf16 [N, 512, dv]. */
+void mo_v_up(const uint16_t* x, const uint16_t* w, int T, int N, int dv, uint16_t* o) {
+  for (int t = 0; t < T; ++t)
+    for (int n = 0; n < N; ++n)
+      for (int v = 0; v < dv; ++v) {
+        double acc = 0.0;
+        for (int l = 0; l < 512; ++l)
+          acc += mo_bf16_decode(x[((size_t)t * N + n) * 512 + l]) * mo_bf16_decode(w[((size_t)n * 512 + l) * dv + v]);
+        o[((size_t)t * N + n) * dv + v] = mo_bf16_encode(acc);
+      }
+}
+
+/* Inverse RoPE of attention output rows ([HALOps-MLA] mla_output_proj: "inverse RoPE
+ * of O"): for each bf16 row [512], elements [rope0, rope0 + 64) hold 32 interleaved
+ * pairs (u, v) rotated by the position's angle; they are rotated back,
+ * (u, v) -> (u c + v s, v c - u s) with (c, s) = freqs[pos, 2i], freqs[pos, 2i+1],
+ * and rounded to bf16. Rows with a position outside [0, max_pos) are copied. */
+void mo_inv_rope(const uint16_t* x, const int32_t* positions, const float* freqs, int max_pos, int rope0, int nrows,
+                 uint16_t* out) {
+  for (int r = 0; r < nrows; ++r) {
+    const uint16_t* xr = x + (size_t)r * 512;
+    uint16_t* o = out + (size_t)r * 512;
+    memcpy(o, xr, 512 * sizeof(uint16_t));
+    const int pos = positions[r];
+    if (pos < 0 || pos >= max_pos) continue;
+    const float* f = freqs + (size_t)pos * 64;
+    for (int i = 0; i < 32; ++i) {
+      const double c = f[2 * i], sn = f[2 * i + 1];
+      const double u = mo_bf16_decode(xr[rope0 + 2 * i]), v = mo_bf16_decode(xr[rope0 + 2 * i + 1]);
+      o[rope0 + 2 * i] = mo_bf16_encode(u * c + v * sn);
+      o[rope0 + 2 * i + 1] = mo_bf16_encode(v * c - u * sn);
+    }
+  }
+}
+
 /* Decoded rows 0..L-1 of one request (block_table row given) -> out [L, dqk]. */
 int mo_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, const int32_t* bt_row,
                  int max_pages, int L, double* out) {

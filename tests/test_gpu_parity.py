@@ -166,6 +166,134 @@ def test_combine_matches_oracle():
     assert np.all(o[1] == 0) and np.all(l[1] == 0)  # single-split request untouched
 
 
+def _bits_to_f64(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("B,sq,N,splits", [(3, 2, 16, (3, 1, 5)), (41, 2, 16, None), (2, 1, 128, (1, 1))])
+def test_combine_v_up_matches_oracle(B, sq, N, splits):
+    """Split combine + value up-projection against the oracle's combine, bf16 rounding
+    and V up-projection (inputs drawn on the host and given to both sides). The second
+    case spans two 64-token blocks with a ragged tail; the third has no split at all."""
+    rng = np.random.default_rng(32 + B)
+    R = sq * N
+    T = B * sq
+    nsplit = np.array(splits if splits is not None else rng.integers(1, 5, B), dtype=np.int32)
+    ns = np.concatenate([[0], np.cumsum(nsplit)]).astype(np.int32)
+    S = int(ns[-1])
+    part_out = (rng.standard_normal((S, R, 512)) * 2).astype(np.float32)
+    part_lse = rng.standard_normal((S, R)).astype(np.float32) * 3
+    part_lse[rng.random((S, R)) < 0.05] = -np.inf          # some empty partials
+    out_bits = torch.from_numpy(rng.standard_normal((T, N, 512)).astype(np.float32)).to(torch.bfloat16)
+    out_bits = out_bits.view(torch.int16).numpy().view(np.uint16)
+    lse_in = rng.standard_normal((T, N)).astype(np.float32)
+    sink = rng.standard_normal(N).astype(np.float32)
+    w_bits = torch.from_numpy((rng.standard_normal((N, 512, 128)) * 0.05).astype(np.float32)).to(torch.bfloat16)
+    w_bits = w_bits.view(torch.int16).numpy().view(np.uint16)
+
+    # oracle: merged latent rows (fp64) of split requests, rounded once to bf16; others as given
+    x_ref = out_bits.copy()
+    merged = {}
+    for b in range(B):
+        if nsplit[b] < 2:
+            continue
+        for r in range(R):
+            o, l = oracle.combine(part_out[ns[b]:ns[b + 1], r].astype(np.float64),
+                                  part_lse[ns[b]:ns[b + 1], r].astype(np.float64), sink=float(sink[r % N]))
+            t, n = b * sq + r // N, r % N
+            merged[(t, n)] = (o, l)
+            x_ref[t, n] = oracle.bf16_encode(o)
+    o_ref = _bits_to_f64(oracle.v_up(x_ref, w_bits))
+
+    split = S > B
+    out = torch.from_numpy(out_bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    lse = torch.from_numpy(lse_in.copy()).cuda()
+    o_v = torch.zeros(T, N, 128, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_combine_v_up(torch.from_numpy(part_out).cuda() if split else None,
+                         torch.from_numpy(part_lse).cuda() if split else None, torch.from_numpy(ns).cuda(), sq, N,
+                         bf16_tensor(w_bits), out, lse, o_v, sink=torch.from_numpy(sink).cuda(), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got_out = out.float().cpu().numpy().astype(np.float64)
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    if merged:
+        keys = list(merged)
+        assert_close(np.stack([got_out[t, n] for t, n in keys]), np.array([got_lse[t, n] for t, n in keys]),
+                     np.stack([merged[k][0] for k in keys]), np.array([merged[k][1] for k in keys]), "merged rows")
+    untouched = np.ones((T, N), bool)
+    for (t, n) in merged:
+        untouched[t, n] = False
+    assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16)[untouched], out_bits[untouched])
+    assert np.array_equal(got_lse[untouched], lse_in[untouched].astype(np.float64))
+    # o_v: the GPU merges in fp32, the oracle in fp64, so a merged latent value may round to the
+    # neighbouring bf16 (2^-8 of its binade); allow a few such flips per dot product, the fp32
+    # accumulation over 512 terms, and half a bf16 step of the result
+    x_abs = np.abs(_bits_to_f64(x_ref))
+    w_abs = np.abs(_bits_to_f64(w_bits))
+    sum_abs = np.einsum("tnl,nlv->tnv", x_abs, w_abs)
+    max_term = x_abs.max(axis=2)[:, :, None] * w_abs.max(axis=1)[None, :, :]
+    tol = np.abs(o_ref) * 2.0 ** -8 + max_term * 2.0 ** -6 + sum_abs * 1e-4
+    got = o_v.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    excess = np.abs(got - o_ref) - tol
+    assert np.all(excess <= 0), f"o_v: worst excess {excess.max():.3g} at {np.unravel_index(np.argmax(excess), excess.shape)}"
+
+
+@pytest.mark.parametrize("B,sq,N,splits", [(3, 2, 64, (3, 1, 5)), (8, 1, 64, None)])
+def test_combine_inv_rope_matches_oracle(B, sq, N, splits):
+    """Split combine + inverse RoPE of elements 448..511 (the DSV4 value row) against the
+    oracle's combine, bf16 rounding and inverse rotation. Both sides round the merged row
+    and the rotated pairs once to bf16 from fp32 (kernel) or fp64 (oracle), so a value may
+    land on the neighbouring bf16: nearly all bits agree and every value is within two bf16
+    steps of its pair's magnitude (rotated elements) or one step (the others)."""
+    rng = np.random.default_rng(70 + B)
+    R, T = sq * N, B * sq
+    nsplit = np.array(splits if splits is not None else rng.integers(1, 4, B), dtype=np.int32)
+    ns = np.concatenate([[0], np.cumsum(nsplit)]).astype(np.int32)
+    S = int(ns[-1])
+    part_out = (rng.standard_normal((S, R, 512)) * 2).astype(np.float32)
+    part_lse = (rng.standard_normal((S, R)) * 3).astype(np.float32)
+    out_bits = torch.from_numpy(rng.standard_normal((T, N, 512)).astype(np.float32)).to(torch.bfloat16)
+    out_bits = out_bits.view(torch.int16).numpy().view(np.uint16)
+    lse_in = rng.standard_normal((T, N)).astype(np.float32)
+    sink = rng.standard_normal(N).astype(np.float32)
+    max_pos = 5000
+    freqs = _rope_table(max_pos)
+    pos = rng.integers(0, max_pos, T).astype(np.int32)
+    pos[-1] = max_pos + 3  # outside the table: merged but not rotated
+
+    x_ref = out_bits.copy()
+    for b in range(B):
+        if nsplit[b] < 2:
+            continue
+        for r in range(R):
+            o, _ = oracle.combine(part_out[ns[b]:ns[b + 1], r].astype(np.float64),
+                                  part_lse[ns[b]:ns[b + 1], r].astype(np.float64), sink=float(sink[r % N]))
+            x_ref[b * sq + r // N, r % N] = oracle.bf16_encode(o)
+    ref = oracle.inv_rope(x_ref.reshape(-1, 512), np.repeat(pos, N), freqs, 448).reshape(T, N, 512)
+
+    split = S > B
+    out = torch.from_numpy(out_bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    lse = torch.from_numpy(lse_in.copy()).cuda()
+    mla.mla_combine_inv_rope(torch.from_numpy(part_out).cuda() if split else None,
+                             torch.from_numpy(part_lse).cuda() if split else None, torch.from_numpy(ns).cuda(), sq, N,
+                             torch.from_numpy(pos).cuda(), torch.from_numpy(freqs).cuda(), out, lse, rope0=448,
+                             sink=torch.from_numpy(sink).cuda())
+    torch.cuda.synchronize()
+    got_bits = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.mean(got_bits != ref) <= 1e-2
+    g, e = _bits_to_f64(got_bits), _bits_to_f64(ref)
+    tol = np.abs(e) * 2.0 ** -7
+    pair = np.sqrt(e[..., 448::2] ** 2 + e[..., 449::2] ** 2)
+    tol[..., 448::2] = pair * 2.0 ** -6
+    tol[..., 449::2] = pair * 2.0 ** -6
+    excess = np.abs(g - e) - tol
+    assert np.all(excess <= 1e-30), f"worst excess {excess.max():.3g} at {np.unravel_index(np.argmax(excess), excess.shape)}"
+    unsplit = np.repeat(nsplit < 2, sq)
+    assert np.array_equal(got_bits[unsplit][..., :448], out_bits[unsplit][..., :448])
+
+
 # ----------------------------------------------------------------------------- decode parity, small shapes
 SMALL = {
     "tiny": lambda: workloads.tiny(),

@@ -564,3 +564,58 @@ def test_norm_rope_write_skips_bad_positions(oracle_lib):
                                     _bf16_bits(np.ones(512)), 1e-6, _freqs(4, 1.0, 0.0), kv, 0, 16)
     assert np.array_equal(out[0, 1152:3 * 1152], kv[0, 1152:3 * 1152])
     assert not np.array_equal(out[0, :1152], kv[0, :1152])
+
+
+# ----------------------------------------------------------------------------- value up-projection
+def test_v_up_identity_weight_selects_latent(oracle_lib):
+    # W_UV[n] = [I_128; 0]: o_v is the first 128 latent elements, bit for bit
+    rng = np.random.default_rng(50)
+    x = _bf16_bits(rng.standard_normal((3, 4, 512)))
+    w = np.zeros((4, 512, 128), np.float32)
+    w[:, np.arange(128), np.arange(128)] = 1.0
+    o = oracle.v_up(x, _bf16_bits(w))
+    assert np.array_equal(o, x[:, :, :128])
+
+
+def test_v_up_matches_torch_bmm_and_is_linear(oracle_lib):
+    # (N, T, L) x (N, L, V) with torch.bmm in float64, then rounded once to bf16; 2 W doubles o exactly
+    rng = np.random.default_rng(51)
+    x = _bf16_bits(rng.standard_normal((5, 3, 512)))
+    w = _bf16_bits(rng.standard_normal((3, 512, 128)) * 0.05)
+    o = oracle.v_up(x, w)
+    ref = torch.bmm(torch.from_numpy(_bf16_val(x)).transpose(0, 1), torch.from_numpy(_bf16_val(w))).transpose(0, 1)
+    ref = ref.numpy()
+    got = _bf16_val(o)
+    # half a bf16 step: 2^-8 of the value's binade
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 * (1 + 1e-12) + 1e-300)
+    o2 = oracle.v_up(x, _bf16_bits(2 * _bf16_val(w)))
+    assert np.array_equal(_bf16_val(o2), 2 * got)
+
+
+# ----------------------------------------------------------------------------- inverse RoPE of the output
+def test_inv_rope_undoes_the_forward_rotation(oracle_lib):
+    # the DSV4 row: kv_norm_rope rotates elements 448..511 forward, inv_rope (written separately)
+    # rotates them back; the two bf16 roundings leave at most one bf16 step per element
+    rng = np.random.default_rng(52)
+    max_pos = 300
+    theta = np.outer(np.arange(max_pos), 10000.0 ** (-np.arange(32) / 32.0))
+    f = _freqs(max_pos, np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32))
+    x = rng.standard_normal((6, 512)).astype(np.float32)
+    pos = np.array([0, 1, 2, 99, 250, 299], np.int32)
+    w = _bf16_bits(np.ones(512))
+    plain = oracle.kv_norm_rope(_bf16_bits(x), pos, w, 1e-6, _freqs(max_pos, 1.0, 0.0), 1)
+    fwd = oracle.kv_norm_rope(_bf16_bits(x), pos, w, 1e-6, f, 1)
+    back = oracle.inv_rope(fwd, pos, f, 448)
+    assert np.array_equal(back[:, :448], plain[:, :448])
+    a, b = _bf16_val(back[:, 448:]), _bf16_val(plain[:, 448:])
+    assert np.all(np.abs(a - b) <= np.abs(b) * 2.0 ** -6 + 2.0 ** -7)
+
+
+def test_inv_rope_quarter_turn_and_bad_position(oracle_lib):
+    # (c, s) = (0, 1): (u, v) -> (v, -u) exactly; a position outside the table copies the row
+    rng = np.random.default_rng(53)
+    x = _bf16_bits(rng.standard_normal((2, 512)))
+    out = oracle.inv_rope(x, np.array([0, 5], np.int32), _freqs(1, 0.0, 1.0), 448)
+    xv, ov = _bf16_val(x), _bf16_val(out)
+    assert np.array_equal(ov[0, 448::2], xv[0, 449::2]) and np.array_equal(ov[0, 449::2], -xv[0, 448::2])
+    assert np.array_equal(out[1], x[1]) and np.array_equal(out[0, :448], x[0, :448])
