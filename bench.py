@@ -413,6 +413,45 @@ def main():
         cir = {"us": us, "alg_bytes": nbytes, "gbps": nbytes / (us * 1e-6) / 1e9,
                "note": "merge of split rows + inverse RoPE of elements 448..511 of every row, in place; L2 flushed"}
 
+    # Sliding-window variant on the same cache (DSV4 row): every token attends over a window of
+    # 96 consecutive cache slots straddling two 64-row pages (two runs), made by mla_swa_plan and
+    # decoded by mla_decode_runs with the planner's top-k schedule (window 96).
+    swa = None
+    if c.layout == 1:
+        window = 96
+        ps = c.page_size
+        npg = kv.shape[0]
+        srng = np.random.default_rng(7)
+        first = srng.integers(0, npg - 2, T) * ps + srng.integers(1, 2 * ps - window + 1, T)
+        widx = (first[:, None] + np.arange(window)[None, :]).astype(np.int32)
+        d_widx = torch.from_numpy(widx).to(dev)
+        d_runs = torch.zeros(T, 4, dtype=torch.int32, device=dev)
+        splan = mla.mla_decode_plan(np.full(c.batch, window, np.int32), c.sq, N, window, 1, num_sms)
+        s_sched = torch.from_numpy(splan.sched).to(dev)
+        s_ns = torch.from_numpy(splan.num_splits).to(dev)
+        s_ws = mla.alloc_workspace(splan.workspace_bytes, dev)
+        s_out = torch.empty_like(out)
+        s_lse = torch.empty_like(lse)
+        tp, td = [], []
+        for k in range(nbd):
+            flush.fill_(k & 0xFF)
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            mla.mla_swa_plan(d_widx, ps, 1, d_runs, stream=stream)
+            e1.record(stream)
+            mla.mla_decode_runs(q, kv, c.layout, ps, d_runs, window, c.sq, c.sm_scale, s_sched, s_ns,
+                                splan.num_partitions, splan.total_splits, s_ws, s_out, s_lse, sink=sink, stream=stream)
+            e2.record(stream)
+            tp.append((e0, e1))
+            td.append((e1, e2))
+        torch.cuda.synchronize(dev)
+        mla.mla_read_status(s_ws)
+        assert np.all(d_runs.cpu().numpy()[:, 3] == window)
+        swa = {"window": window, "tokens": T, "us_plan": statistics.mean(a.elapsed_time(b) for a, b in tp) * 1e3,
+               "us_decode": statistics.mean(a.elapsed_time(b) for a, b in td) * 1e3,
+               "note": "per token 96 consecutive cache slots over two pages (two runs); plan + decode (+ combine); "
+                       "L2 flushed"}
+
     # The fused RMSNorm + RoPE + write of the same new rows (raw rows in, cache rows out), timed
     # alone. It rewrites those slots; the e2e loop below writes them back with mla_kv_write.
     kvnr = None
@@ -589,6 +628,7 @@ def main():
             "kv_write_norm_rope": kvnr,
             "combine_v_up": cvu,
             "combine_inv_rope": cir,
+            "swa_decode": swa,
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                     "steps": args.e2e_steps, "matches_device_path": e2e_matches,

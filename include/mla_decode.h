@@ -200,6 +200,37 @@ int mla_decode_static_workspace(const void* q, const void* kv_cache, mla_kv_layo
                                 uint32_t* status_out, void* stream);
 
 /*
+ * Sliding-window runs (device): compress each token's window of cache slots into at
+ * most two runs of consecutive slots ("MLA" API page of HALOps, mla_attention_plan).
+ *  kv_indices   device int32 [num_tokens, topk]: the window's cache slots
+ *               (page * page_size + offset); columns past a token's length are ignored.
+ *  topk_lengths device int32 [num_tokens] or NULL (every window has topk rows); clamped
+ *               to [0, topk].
+ *  kv_run_step  1 or -1: the slot step between consecutive window rows.
+ *  runs         device int32 [num_tokens, 4], 16-byte aligned: (slot0, len0, slot1, rows).
+ * A run continues while the next slot equals the previous one plus kv_run_step and lies on
+ * the same page. A window of more than two runs is cut to its first row (rows = 1). Each
+ * run is stored from its lowest slot upwards: row g < len0 is slot slot0 + g, row g >= len0
+ * is slot slot1 + g - len0, for g < rows. An empty window gives (0, 0, 0, 0).
+ */
+int mla_swa_plan(const int32_t* kv_indices, const int32_t* topk_lengths, int32_t num_tokens, int32_t topk,
+                 int32_t page_size, int32_t kv_run_step, int32_t* runs, void* stream);
+
+/*
+ * Decode over window runs (device): as mla_decode, with each query token attending over
+ * the rows of its runs (mla_swa_plan) instead of a request's context. Slots address the
+ * cache directly (no block_table, no cache_seqlens); a slot outside the cache is skipped
+ * and counted in the status word like a bad page. `window` is the largest rows value
+ * (the topk of mla_swa_plan) and is the topk given to mla_decode_plan for the schedule.
+ * Requests are independent tokens' windows: q_tokens_per_req > 1 needs num_heads % 64 == 0.
+ */
+int mla_decode_runs(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
+                    const int32_t* runs, int32_t window, int32_t batch, int32_t q_tokens_per_req, int32_t num_heads,
+                    float sm_scale, const float* sink, const int32_t* sched, const int32_t* num_splits,
+                    int32_t num_partitions, int32_t total_splits, void* workspace, size_t workspace_bytes, void* out,
+                    float* lse, uint32_t flags, void* stream);
+
+/*
  * Split combine (device): for every request whose split count
  * (num_splits[b+1] - num_splits[b]) is at least 2, merge its partials by
  * log-sum-exp — lse = ln sum_s e^(lse_s), out = sum_s e^(lse_s - lse) o_s, a

@@ -48,7 +48,8 @@ class _PlanInfo(ctypes.Structure):
                 ("max_splits", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
 
 
-EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_decode_static_workspace", "mla_combine",
+EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_decode_runs", "mla_swa_plan",
+           "mla_decode_static_workspace", "mla_combine",
            "mla_combine_v_up", "mla_combine_inv_rope", "mla_kv_write", "mla_kv_write_norm_rope", "mla_kv_gather", "mla_workspace_init", "mla_read_status",
            "mla_last_error"]
 STATIC_WORKSPACE_BYTES = 64 << 20
@@ -71,6 +72,9 @@ def load(path: str | None = None):
         lib.mla_decode_plan.argtypes = [V, I32, I32, I32, I32, I32, I32, V, I32, V, ctypes.POINTER(_PlanInfo)]
         lib.mla_decode.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32, V, V, I32, I32,
                                    V, SZ, V, V, ctypes.c_uint32, V]
+        lib.mla_decode_runs.argtypes = [V, V, I32, I64, I32, V, I32, I32, I32, I32, F32, V, V, V, I32, I32, V, SZ, V,
+                                        V, ctypes.c_uint32, V]
+        lib.mla_swa_plan.argtypes = [V, V, I32, I32, I32, I32, V, V]
         lib.mla_decode_static_workspace.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32,
                                                     V, V, I32, I32, V, V, V, V]
         lib.mla_combine.argtypes = [V, V, V, I32, I32, I32, V, V, V, V]
@@ -172,6 +176,28 @@ def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seql
                              num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
                              (1 if skip_combine else 0) | (0x80000000 if _test_withhold_signal else 0),
                              _stream(stream)))
+
+
+def mla_swa_plan(kv_indices, page_size: int, kv_run_step: int, runs, topk_lengths=None, stream=None):
+    """Window runs: kv_indices int32 [T, topk] cache slots -> runs int32 [T, 4] (slot0, len0, slot1, rows)."""
+    _require_cuda(kv_indices, runs, topk_lengths)
+    T, topk = kv_indices.shape
+    _check(load().mla_swa_plan(_ptr(kv_indices), _ptr(topk_lengths), T, topk, page_size, kv_run_step, _ptr(runs),
+                               _stream(stream)))
+
+
+def mla_decode_runs(q, kv_cache, layout: int, page_size: int, runs, window: int, q_tokens_per_req: int,
+                    sm_scale: float, sched, num_splits, num_partitions: int, total_splits: int, workspace, out, lse,
+                    sink=None, skip_combine: bool = False, stream=None):
+    """Decode where token t attends over the rows of its window runs (runs int32 [T, 4] from
+    mla_swa_plan); the plan comes from mla_decode_plan with topk = window."""
+    _require_cuda(q, kv_cache, runs, sched, num_splits, workspace, out, lse, sink)
+    T, N, D = q.shape
+    B = T // q_tokens_per_req
+    _check(load().mla_decode_runs(_ptr(q), _ptr(kv_cache), layout, kv_cache.shape[0], page_size, _ptr(runs), window,
+                                  B, q_tokens_per_req, N, float(sm_scale), _ptr(sink), _ptr(sched), _ptr(num_splits),
+                                  num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out),
+                                  _ptr(lse), 1 if skip_combine else 0, _stream(stream)))
 
 
 def mla_decode_static_workspace(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens,

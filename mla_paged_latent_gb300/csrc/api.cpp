@@ -147,14 +147,27 @@ int mla_decode_plan(const int32_t* cache_seqlens, int32_t batch, int32_t q_token
   return MLA_OK;
 }
 
-int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
-               const int32_t* block_table, int32_t max_pages, const int32_t* cache_seqlens, int32_t batch,
-               int32_t q_tokens_per_req, int32_t num_heads, float sm_scale, const float* sink,
-               const int32_t* indices, int32_t topk, int32_t causal, const int32_t* sched,
-               const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
-               size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream) {
-  if (!q || !kv_cache || !block_table || !cache_seqlens || !sched || !num_splits || !workspace || !out || !lse)
+}  // extern "C"
+
+namespace {
+// Shared body of mla_decode and mla_decode_runs. runs != NULL selects the run-window mode:
+// candidates are the rows of each token's (at most two) slot runs, topk is the window, and
+// block_table / cache_seqlens are not used.
+int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
+                const int32_t* block_table, int32_t max_pages, const int32_t* cache_seqlens, int32_t batch,
+                int32_t q_tokens_per_req, int32_t num_heads, float sm_scale, const float* sink,
+                const int32_t* indices, const int32_t* runs, int32_t topk, int32_t causal, const int32_t* sched,
+                const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
+                size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream) {
+  if (!q || !kv_cache || !sched || !num_splits || !workspace || !out || !lse)
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: NULL pointer argument");
+  if (runs == nullptr && (!block_table || !cache_seqlens))
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode: NULL pointer argument");
+  if (runs != nullptr) {
+    if (indices != nullptr || topk < 1 || causal)
+      return fail(MLA_ERR_INVALID_ARG, "mla_decode_runs: window must be >= 1, with no indices and no causal mask");
+    max_pages = 1;
+  }
   int64_t row_bytes, page_bytes;
   int dqk;
   if (layout_geometry(layout, page_size, &row_bytes, &page_bytes, &dqk) != 0)
@@ -167,9 +180,9 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
   if (R > 4096) return fail(MLA_ERR_UNSUPPORTED, "mla_decode: q_tokens_per_req * num_heads = %lld > 4096", (long long)R);
   if (static_cast<int64_t>(batch) * R >= (1ll << 31))
     return fail(MLA_ERR_UNSUPPORTED, "mla_decode: too many query rows");
-  if ((indices != nullptr) != (topk > 0))
+  if (runs == nullptr && (indices != nullptr) != (topk > 0))
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: indices must be given exactly when topk > 0 (topk=%d)", topk);
-  if (indices != nullptr && q_tokens_per_req > 1 && num_heads % mla::kGroupRows != 0)
+  if ((indices != nullptr || runs != nullptr) && q_tokens_per_req > 1 && num_heads % mla::kGroupRows != 0)
     return fail(MLA_ERR_UNSUPPORTED, "mla_decode: sparse decode with several tokens needs heads %% 64 == 0");
   if (total_splits < batch) return fail(MLA_ERR_INVALID_ARG, "mla_decode: total_splits %d < batch %d", total_splits, batch);
   if (!(sm_scale > 0.f) || !(sm_scale < 1e30f))
@@ -203,7 +216,7 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the q tensor map failed (%d)", (int)r);
   }
-  const bool tma_kv = (layout == MLA_KV_BF16_576) && indices == nullptr;
+  const bool tma_kv = (layout == MLA_KV_BF16_576) && indices == nullptr && runs == nullptr;
   if (tma_kv) {
     const cuuint64_t dims[3] = {576, static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(num_pages)};
     const cuuint64_t strides[2] = {1152, static_cast<cuuint64_t>(page_bytes)};
@@ -225,6 +238,7 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
   p.seqlens = cache_seqlens;
   p.sink = sink;
   p.indices = indices;
+  p.runs = runs;
   p.sched = sched;
   p.num_splits = num_splits;
   p.out = static_cast<uint16_t*>(out);
@@ -264,6 +278,47 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
                             lse, s);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode: combine launch");
   }
+  return MLA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
+               const int32_t* block_table, int32_t max_pages, const int32_t* cache_seqlens, int32_t batch,
+               int32_t q_tokens_per_req, int32_t num_heads, float sm_scale, const float* sink,
+               const int32_t* indices, int32_t topk, int32_t causal, const int32_t* sched,
+               const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
+               size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream) {
+  return decode_impl(q, kv_cache, layout, num_pages, page_size, block_table, max_pages, cache_seqlens, batch,
+                     q_tokens_per_req, num_heads, sm_scale, sink, indices, nullptr, topk, causal, sched, num_splits,
+                     num_partitions, total_splits, workspace, workspace_bytes, out, lse, flags, stream);
+}
+
+int mla_decode_runs(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
+                    const int32_t* runs, int32_t window, int32_t batch, int32_t q_tokens_per_req, int32_t num_heads,
+                    float sm_scale, const float* sink, const int32_t* sched, const int32_t* num_splits,
+                    int32_t num_partitions, int32_t total_splits, void* workspace, size_t workspace_bytes, void* out,
+                    float* lse, uint32_t flags, void* stream) {
+  if (runs == nullptr) return fail(MLA_ERR_INVALID_ARG, "mla_decode_runs: runs is NULL");
+  if (reinterpret_cast<uintptr_t>(runs) & 15u)
+    return fail(MLA_ERR_INVALID_ARG, "mla_decode_runs: runs must be 16-byte aligned");
+  return decode_impl(q, kv_cache, layout, num_pages, page_size, nullptr, 1, nullptr, batch, q_tokens_per_req,
+                     num_heads, sm_scale, sink, nullptr, runs, window, 0, sched, num_splits, num_partitions,
+                     total_splits, workspace, workspace_bytes, out, lse, flags, stream);
+}
+
+int mla_swa_plan(const int32_t* kv_indices, const int32_t* topk_lengths, int32_t num_tokens, int32_t topk,
+                 int32_t page_size, int32_t kv_run_step, int32_t* runs, void* stream) {
+  if (!kv_indices || !runs) return fail(MLA_ERR_INVALID_ARG, "mla_swa_plan: NULL pointer argument");
+  if (num_tokens < 1 || topk < 1) return fail(MLA_ERR_INVALID_ARG, "mla_swa_plan: num_tokens and topk must be >= 1");
+  if (!pow2(page_size)) return fail(MLA_ERR_INVALID_ARG, "mla_swa_plan: page_size %d not a power of two", page_size);
+  if (reinterpret_cast<uintptr_t>(runs) & 15u) return fail(MLA_ERR_INVALID_ARG, "mla_swa_plan: runs must be 16-byte aligned");
+  if (kv_run_step != 1 && kv_run_step != -1)
+    return fail(MLA_ERR_INVALID_ARG, "mla_swa_plan: kv_run_step must be 1 or -1 (got %d)", kv_run_step);
+  cudaError_t e = mla::launch_swa_plan(kv_indices, topk_lengths, num_tokens, topk, page_size, kv_run_step, runs,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_swa_plan: launch");
   return MLA_OK;
 }
 

@@ -91,6 +91,63 @@ __global__ void __launch_bounds__(256) combine_inv_rope_kernel(
   }
 }
 
+// ----------------------------------------------------------------------------- window runs
+// One warp per token: compress its window (kv_indices[t, 0 .. len), len = topk_lengths[t]
+// clamped to [0, topk], or topk) into at most two runs of consecutive cache slots ("MLA" API
+// page of HALOps, mla_attention_plan). A run continues while the next slot is the previous
+// one plus kv_run_step and lies on the same page; a window of more than two runs is cut to
+// its first row. Each run is stored from its lowest slot upwards (attention does not depend
+// on the order of its rows): row g < len0 is slot slot0 + g, row g >= len0 slot1 + g - len0.
+// The lanes read 32 window entries at a time and find the run breaks with one ballot.
+__global__ void __launch_bounds__(128) swa_plan_kernel(const int32_t* __restrict__ idx,
+                                                       const int32_t* __restrict__ lens, int T, int topk,
+                                                       int log2_ps, int step, int4* __restrict__ runs) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int len = lens ? lens[t] : topk;
+  len = len < 0 ? 0 : (len > topk ? topk : len);
+  if (len == 0) {
+    if (lane == 0) runs[t] = make_int4(0, 0, 0, 0);
+    return;
+  }
+  const int32_t* w = idx + (int64_t)t * topk;
+  const int first = w[0];
+  int nb = 0, b1 = len, s1 = 0;  // breaks found; row and slot of the first break
+  int carry = first;
+  for (int base = 0; base < len && nb < 2; base += 32) {
+    const int g = base + lane;
+    const bool valid = g < len;
+    const int cur = valid ? w[g] : 0;
+    int prev = __shfl_up_sync(0xffffffffu, cur, 1);
+    if (lane == 0) prev = carry;
+    const bool brk = valid && g > 0 && (cur != prev + step || (cur >> log2_ps) != (prev >> log2_ps));
+    unsigned m = __ballot_sync(0xffffffffu, brk);
+    while (m != 0u && nb < 2) {
+      const int l = __ffs(m) - 1;
+      const int v = __shfl_sync(0xffffffffu, cur, l);
+      if (nb == 0) {
+        b1 = base + l;
+        s1 = v;
+      }
+      ++nb;
+      m &= m - 1u;
+    }
+    carry = __shfl_sync(0xffffffffu, cur, 31);
+  }
+  if (lane != 0) return;
+  if (nb >= 2) {
+    runs[t] = make_int4(first, 1, first, 1);
+    return;
+  }
+  const int c0 = b1;  // len when the window is one run
+  const int lo0 = step > 0 ? first : first - (c0 - 1);
+  const int lo1 = nb == 1 ? (step > 0 ? s1 : s1 - (len - b1 - 1)) : lo0 + c0;
+  runs[t] = make_int4(lo0, c0, lo1, len);
+}
+
 // ----------------------------------------------------------------------------- kv write
 // 448 * 2^e as fp32 (exact; +inf once it exceeds the fp32 range).
 __device__ __forceinline__ float pow2x448(int e) {
@@ -300,6 +357,14 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
   dim3 grid((rows_per_req + 7) / 8, batch);
   return launch_pdl(combine_kernel, grid, dim3(256), 0, stream, part_out, part_lse, num_splits, rows_per_req, heads,
                     sink, out, lse);
+}
+
+cudaError_t launch_swa_plan(const int32_t* kv_indices, const int32_t* topk_lengths, int num_tokens, int topk,
+                            int page_size, int kv_run_step, int32_t* runs, cudaStream_t stream) {
+  int lg = 0;
+  while ((1 << lg) < page_size) ++lg;
+  return launch_pdl(swa_plan_kernel, dim3((num_tokens + 3) / 4), dim3(128), 0, stream, kv_indices, topk_lengths,
+                    num_tokens, topk, lg, kv_run_step, reinterpret_cast<int4*>(runs));
 }
 
 cudaError_t launch_combine_inv_rope(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,

@@ -130,7 +130,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const bool sparse = P.indices != nullptr;
+  // candidates listed per token: top-k positions (indices) or the rows of its slot runs
+  // (gathered variants only: the TMA variant never sees either)
+  const int32_t* const runs = TMA_KV ? nullptr : P.runs;
+  const bool sparse = P.indices != nullptr || runs != nullptr;
 
   if (tid == 0) {
     mbar_init(bar(kQFull), 1);
@@ -364,8 +367,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           rows = rows > P.qbox_rows ? P.qbox_rows : rows;
           if (rows > 0) prefetch_l2_bulk(P.q + row0 * (NS * 64), static_cast<uint32_t>(rows * NS * 64 * 2));
         }
-        const int L = P.seqlens[r];
+        const int L = runs ? 0x7fffffff : P.seqlens[r];
         const int tok = r * P.sq + (g * kGroupRows) / P.heads;
+        const int4 rn = runs ? reinterpret_cast<const int4*>(runs)[tok] : make_int4(0, 0, 0, 0);
         for (int j = lo; j < hi; ++j, ++pit) {
           const uint64_t t0 = globaltimer();
           while (pit >= *reinterpret_cast<volatile int*>(&misc->progress) + ahead) {
@@ -379,14 +383,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int kk = j * kBlockRows + lane + 32 * h;
-              pos[h] = kk < P.topk ? P.indices[static_cast<int64_t>(tok) * P.topk + kk] : -1;
+              if (runs) pos[h] = kk < rn.w ? (kk < rn.y ? rn.x + kk : rn.z + kk - rn.y) : -1;
+              else pos[h] = kk < P.topk ? P.indices[static_cast<int64_t>(tok) * P.topk + kk] : -1;
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               page[h] = -1;
               if (pos[h] < 0 || pos[h] >= L) continue;
               const int pi = pos[h] >> P.log2_ps;
-              page[h] = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
+              if (runs) page[h] = pi;  // run slots are cache slots: page * page_size + offset
+              else page[h] = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int nq = (rows_g + 15) & ~15;
       for_each_unit(P, part, [&](int r, int lo, int hi, int sidx) {
         if (stop) return;
-        const int L = P.seqlens[r];
+        const int L = runs ? 0x7fffffff : P.seqlens[r];
         const int grow = g * kGroupRows + row;          // query row within the request
         const bool valid_row = row_thread && row < rows_g;
         const int tok = grow / P.heads;
@@ -671,8 +677,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int part = w / G, g = w % G;
       for_each_unit(P, part, [&](int r, int lo, int hi, int) {
         if (*abort_flag) return;
-        const int L = P.seqlens[r];
+        const int L = runs ? 0x7fffffff : P.seqlens[r];
         const int tok = r * P.sq + (g * kGroupRows) / P.heads;   // sparse: the group's token
+        const int4 rn = runs ? reinterpret_cast<const int4*>(runs)[tok] : make_int4(0, 0, 0, 0);
         // The address chain of a row (top-k index -> block_table entry -> row) runs two
         // tiles ahead of the conversion: the index of tile j + 2 and the page of tile j + 1
         // are loaded while tile j is converted, so only a unit's first tile waits for them.
@@ -680,6 +687,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           if (j >= hi) return -1;
           if (sparse) {
             const int kk = j * kBlockRows + crow;
+            if (runs) return kk < rn.w ? (kk < rn.y ? rn.x + kk : rn.z + kk - rn.y) : -1;
             return kk < P.topk ? P.indices[(int64_t)tok * P.topk + kk] : -1;
           }
           return j * kBlockRows + crow;
@@ -687,7 +695,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         auto row_page = [&](int pos) -> int {  // its page; -1 if no row, -2 if the entry is bad
           if (pos < 0 || pos >= L) return -1;
           const int pi = pos >> P.log2_ps;
-          const int page = pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1;
+          // run slots are cache slots (page * page_size + offset), not positions of the request
+          const int page = runs ? pi : (pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1);
           return (page < 0 || page >= P.num_pages) ? -2 : page;
         };
         int pos_a = row_pos(lo), pos_b = row_pos(lo + 1);

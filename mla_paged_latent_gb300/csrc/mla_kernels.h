@@ -19,6 +19,7 @@ struct DecodeParams {
   const int32_t* seqlens;         // [batch]
   const float* sink;              // [heads] or null
   const int32_t* indices;         // [T, topk] or null
+  const int32_t* runs;            // [T, 4] (slot0, len0, slot1, rows) or null: run-window mode
   const int32_t* sched;           // [num_partitions, 8]
   const int32_t* num_splits;      // [batch + 1]
   uint16_t* out;                  // bf16 [T, heads, 512]
@@ -65,6 +66,9 @@ cudaError_t launch_kv_write_norm_rope(const uint16_t* raw, const int32_t* slots,
                                      const uint16_t* norm_weight, float eps, const float* freqs, int max_pos, int n,
                                      uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
                                      cudaStream_t stream);
+
+cudaError_t launch_swa_plan(const int32_t* kv_indices, const int32_t* topk_lengths, int num_tokens, int topk,
+                            int page_size, int kv_run_step, int32_t* runs, cudaStream_t stream);
 
 cudaError_t launch_combine_inv_rope(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
                                     int sq, int heads, const float* sink, const int32_t* positions, const float* freqs,

@@ -92,6 +92,8 @@ def _load():
         lib.mo_v_up.restype = None
         lib.mo_inv_rope.argtypes = [P, P, P, i32, i32, i32, P]
         lib.mo_inv_rope.restype = None
+        lib.mo_swa_plan.argtypes = [P, P, i32, i32, i32, i32, P]
+        lib.mo_swa_plan.restype = None
         _lib = lib
         return lib
 
@@ -286,6 +288,45 @@ def inv_rope(x_bits, positions, freqs, rope0: int = 448) -> np.ndarray:
     out = np.zeros_like(x)
     lib.mo_inv_rope(_ptr(x), _ptr(pos), _ptr(f), f.shape[0], rope0, x.shape[0], _ptr(out))
     return out
+
+
+def swa_plan(kv_indices, page_size: int, step: int, topk_lengths=None) -> np.ndarray:
+    """Window runs: kv_indices int32 [T, topk] -> int32 [T, 4] (slot0, len0, slot1, rows)."""
+    lib = _load()
+    idx = _c(kv_indices, np.int32)
+    T, topk = idx.shape
+    lens = _c(topk_lengths, np.int32)
+    runs = np.zeros((T, 4), np.int32)
+    lib.mo_swa_plan(_ptr(idx), _ptr(lens), T, topk, page_size, step, _ptr(runs))
+    return runs
+
+
+def run_slots(run) -> np.ndarray:
+    """The cache slots of one token's runs (slot0, len0, slot1, rows), in row order."""
+    s0, l0, s1, rows = (int(v) for v in run)
+    g = np.arange(rows)
+    return np.where(g < l0, s0 + g, s1 + g - l0).astype(np.int64)
+
+
+def decode_runs(q_bits, kv_cache, layout: int, page_size: int, runs, sm_scale: float, sink=None):
+    """Attention of every (token, head) over the rows of its token's runs: slots address
+    the cache directly; slots outside it are skipped. Returns (out [T, N, 512], lse [T, N])."""
+    q = _c(q_bits, np.uint16)
+    T, N, dqk = q.shape
+    info = layout_info(layout, page_size)
+    kv = np.ascontiguousarray(kv_cache, dtype=np.uint8)
+    npages = kv.shape[0]
+    out = np.zeros((T, N, 512))
+    lse = np.zeros((T, N))
+    qf = bf16_decode(q.reshape(-1)).reshape(T, N, dqk)
+    for t in range(T):
+        slots = [s for s in run_slots(runs[t]) if 0 <= s < npages * page_size]
+        rows = np.array([decode_row(kv, layout, page_size, s // page_size, s % page_size) for s in slots]
+                        ).reshape(-1, info["dqk"])
+        for n in range(N):
+            o, l = attend(qf[t, n], rows, 512, sm_scale, None if sink is None else float(sink[n]))
+            out[t, n], lse[t, n] = o, l
+    return out, lse
 
 
 def kv_gather(kv_cache, layout, page_size, block_table_row, length) -> np.ndarray:

@@ -490,6 +490,56 @@ void mo_inv_rope(const uint16_t* x, const int32_t* positions, const float* freqs
   }
 }
 
+/* Sliding-window runs ([HALOps-MLA] mla_attention_plan): token t's window is
+ * kv_indices[t, 0 .. len), len = lengths[t] clamped to [0, topk] (topk when lengths is
+ * NULL). Walking it in order, a run continues while the next slot is the previous one
+ * plus step and on the same page (slot / page_size); a window of more than two runs is
+ * cut to its first row. Output (slot0, len0, slot1, rows) per token, each run given by its
+ * lowest slot (row g < len0 -> slot0 + g, else slot1 + g - len0); an empty window gives
+ * zeros; a single run gives slot1 = slot0 + len0. */
+void mo_swa_plan(const int32_t* idx, const int32_t* lengths, int T, int topk, int page_size, int step, int32_t* runs) {
+  for (int t = 0; t < T; ++t) {
+    const int32_t* w = idx + (size_t)t * topk;
+    int32_t* o = runs + (size_t)t * 4;
+    int len = lengths ? lengths[t] : topk;
+    if (len < 0) len = 0;
+    if (len > topk) len = topk;
+    if (len == 0) {
+      o[0] = o[1] = o[2] = o[3] = 0;
+      continue;
+    }
+    /* split the window into maximal runs */
+    int starts[3], counts[3], n = 0;
+    for (int g = 0; g < len && n <= 2; ++g) {
+      const int cont = g > 0 && w[g] == w[g - 1] + step &&
+                       (int)floor((double)w[g] / page_size) == (int)floor((double)w[g - 1] / page_size);
+      if (cont) {
+        counts[n - 1] += 1;
+      } else {
+        if (n == 2) {
+          n = 3;
+          break;
+        }
+        starts[n] = w[g];
+        counts[n] = 1;
+        n += 1;
+      }
+    }
+    if (n > 2) {
+      o[0] = w[0];
+      o[1] = 1;
+      o[2] = w[0];
+      o[3] = 1;
+      continue;
+    }
+    const int lo0 = step > 0 ? starts[0] : starts[0] - (counts[0] - 1);
+    o[0] = lo0;
+    o[1] = counts[0];
+    o[2] = n == 2 ? (step > 0 ? starts[1] : starts[1] - (counts[1] - 1)) : lo0 + counts[0];
+    o[3] = len;
+  }
+}
+
 /* Decoded rows 0..L-1 of one request (block_table row given) -> out [L, dqk]. */
 int mo_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, const int32_t* bt_row,
                  int max_pages, int L, double* out) {

@@ -294,6 +294,76 @@ def test_combine_inv_rope_matches_oracle(B, sq, N, splits):
     assert np.array_equal(got_bits[unsplit][..., :448], out_bits[unsplit][..., :448])
 
 
+def _windows(rng, T, window, ps, num_slots):
+    """Token windows of cache slots: contiguous ranges (ascending or descending, some crossing
+    a page), some cut short by a length, and some made of three runs (cut to one row)."""
+    idx = np.full((T, window), -1, np.int32)
+    lens = np.zeros(T, np.int32)
+    steps = np.zeros(T, np.int32)
+    for t in range(T):
+        n = int(rng.integers(1, window + 1)) if t % 5 else window
+        step = 1 if t % 3 else -1
+        start = int(rng.integers(n, num_slots - n))
+        sl = start + step * np.arange(n)
+        if t % 7 == 3 and n > 4:          # three runs
+            sl[n // 3:] += 2 * step * ps
+            sl[2 * n // 3:] += 2 * step * ps
+            sl = np.clip(sl, 0, num_slots - 1)
+        idx[t, :n] = sl
+        lens[t] = n
+        steps[t] = step
+    return idx, lens, steps
+
+
+@pytest.mark.parametrize("ps,step", [(16, 1), (64, -1), (128, 1)])
+def test_swa_plan_bit_exact(ps, step):
+    rng = np.random.default_rng(80 + ps)
+    T, window = 300, 160
+    # windows listed both ways: those against `step` fall apart into many runs and are cut
+    idx, lens, _ = _windows(rng, T, window, ps, 40 * ps)
+    lens[::11] = 0
+    ref = oracle.swa_plan(idx, ps, step, lens)
+    runs = torch.zeros(T, 4, dtype=torch.int32, device="cuda")
+    mla.mla_swa_plan(torch.from_numpy(idx).cuda(), ps, step, runs, topk_lengths=torch.from_numpy(lens).cuda())
+    assert np.array_equal(runs.cpu().numpy(), ref)
+    ref_nolen = oracle.swa_plan(idx, ps, step)
+    mla.mla_swa_plan(torch.from_numpy(idx).cuda(), ps, step, runs)
+    assert np.array_equal(runs.cpu().numpy(), ref_nolen)
+
+
+@pytest.mark.parametrize("layout,heads", [(1, 64), (0, 128), (2, 64)])
+def test_decode_runs_matches_oracle(layout, heads):
+    """Sliding-window decode: each token over the rows of its runs (from mla_swa_plan on the
+    GPU, checked against the oracle's runs first), split by the planner like a top-k decode."""
+    ps, window = 64, 96
+    cfg = (workloads.dsv4 if layout == 1 else workloads.dsv3)(
+        batch=24, seqlens=tuple([300] * 24), len_dist="fixed", page_size=ps, heads=heads, layout=layout)
+    w = workloads.generate(cfg)
+    c = w.cfg
+    rng = np.random.default_rng(90 + layout)
+    T = c.batch
+    num_slots = w.kv_cache.shape[0] * ps
+    idx, lens, steps = _windows(rng, T, window, ps, num_slots)
+    # one step per call: ascending windows here, descending ones reversed into ascending order
+    idx = np.array([r if steps[t] > 0 else np.concatenate([r[:lens[t]][::-1], r[lens[t]:]])
+                    for t, r in enumerate(idx)], np.int32)
+    ref_runs = oracle.swa_plan(idx, ps, 1, lens)
+    runs = torch.zeros(T, 4, dtype=torch.int32, device="cuda")
+    mla.mla_swa_plan(torch.from_numpy(idx).cuda(), ps, 1, runs, topk_lengths=torch.from_numpy(lens).cuda())
+    assert np.array_equal(runs.cpu().numpy(), ref_runs)
+    plan = mla.mla_decode_plan(np.full(T, window, np.int32), 1, heads, window, 2, 152)
+    ws = mla.alloc_workspace(plan.workspace_bytes)
+    out = torch.empty(T, heads, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(T, heads, dtype=torch.float32, device="cuda")
+    sink = None if w.sink is None else torch.from_numpy(w.sink).cuda()
+    mla.mla_decode_runs(bf16_tensor(w.q), torch.from_numpy(w.kv_cache).cuda(), layout, ps, runs, window, 1,
+                        c.sm_scale, torch.from_numpy(plan.sched).cuda(), torch.from_numpy(plan.num_splits).cuda(),
+                        plan.num_partitions, plan.total_splits, ws, out, lse, sink=sink)
+    mla.mla_read_status(ws)
+    ref_out, ref_lse = oracle.decode_runs(w.q, w.kv_cache, layout, ps, ref_runs, c.sm_scale, sink=w.sink)
+    assert_close(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, f"runs layout {layout}")
+
+
 # ----------------------------------------------------------------------------- decode parity, small shapes
 SMALL = {
     "tiny": lambda: workloads.tiny(),

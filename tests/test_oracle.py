@@ -619,3 +619,52 @@ def test_inv_rope_quarter_turn_and_bad_position(oracle_lib):
     xv, ov = _bf16_val(x), _bf16_val(out)
     assert np.array_equal(ov[0, 448::2], xv[0, 449::2]) and np.array_equal(ov[0, 449::2], -xv[0, 448::2])
     assert np.array_equal(out[1], x[1]) and np.array_equal(out[0, :448], x[0, :448])
+
+
+# ----------------------------------------------------------------------------- sliding-window runs
+def test_swa_plan_hand_built_windows(oracle_lib):
+    # page size 16; each case worked by hand from the rule (runs of +step within one page,
+    # more than two runs -> the first row only, runs stored from their lowest slot)
+    pad = -1
+    cases = [
+        ([32 + g for g in range(16)], 16, 1, (32, 16, 48, 16)),          # one page, one run
+        ([40 + g for g in range(16)], 16, 1, (40, 8, 48, 16)),           # crosses into the next page
+        ([40, 41, 42, 60, 61, 100] + [pad] * 10, 6, 1, (40, 1, 40, 1)),  # three runs: cut
+        ([55 - g for g in range(16)], 16, -1, (48, 8, 40, 16)),          # descending across a page
+        ([5, 6, pad, pad] + [pad] * 12, 2, 1, (5, 2, 7, 2)),             # padding past the length
+        ([3, 7, 8] + [pad] * 13, 3, 1, (3, 1, 7, 3)),                    # a gap inside one page
+        ([9] * 16, 0, 1, (0, 0, 0, 0)),                                  # empty window
+        ([20, 19, 18, 30] + [pad] * 12, 4, -1, (18, 3, 30, 4)),          # descending run, then one row
+    ]
+    idx = np.array([c[0] for c in cases], np.int32)
+    lens = np.array([c[1] for c in cases], np.int32)
+    for step in (1, -1):
+        sel = [i for i, c in enumerate(cases) if c[2] == step]
+        runs = oracle.swa_plan(idx[sel], 16, step, lens[sel])
+        for k, i in enumerate(sel):
+            assert tuple(runs[k]) == cases[i][3], (i, tuple(runs[k]))
+
+
+def test_swa_plan_lengths_clamp_and_default(oracle_lib):
+    idx = np.tile(np.arange(100, 108, dtype=np.int32), (3, 1))
+    assert tuple(oracle.swa_plan(idx[:1], 64, 1)[0]) == (100, 8, 108, 8)          # no lengths: topk rows
+    runs = oracle.swa_plan(idx, 64, 1, np.array([-3, 50, 3], np.int32))
+    assert tuple(runs[0]) == (0, 0, 0, 0) and tuple(runs[1]) == (100, 8, 108, 8) and tuple(runs[2]) == (100, 3, 103, 3)
+
+
+def test_decode_over_runs_equals_dense_and_is_order_free(oracle_lib):
+    # a request whose positions 0..L-1 sit on consecutive slots of pages 3 and 4: its window of
+    # all L rows (listed ascending or descending) gives the dense decode of that request
+    w = workloads.generate(workloads.tiny())
+    c = w.cfg
+    ps = c.page_size
+    L = 20
+    kv = w.kv_cache
+    bt = np.array([[3, 4] + [-1] * (w.block_table.shape[1] - 2)], np.int32)
+    q = w.q[:1]
+    dense_out, dense_lse = oracle.mla_decode(q, kv, c.layout, ps, bt, np.array([L], np.int32), 1, c.sm_scale)
+    slots = np.array([3 * ps + p for p in range(L)], np.int32)
+    for step, order in ((1, slots), (-1, slots[::-1].copy())):
+        runs = oracle.swa_plan(order[None, :], ps, step)
+        out, lse = oracle.decode_runs(q, kv, c.layout, ps, runs, c.sm_scale)
+        assert np.allclose(out, dense_out, rtol=1e-12, atol=1e-12) and np.allclose(lse, dense_lse, rtol=1e-12)
