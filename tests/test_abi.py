@@ -152,3 +152,42 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         mla.mla_kv_write(torch.zeros(4, 576, dtype=torch.bfloat16), torch.zeros(4, dtype=torch.int32),
                          torch.zeros(2, 100, dtype=torch.uint8), 0, 16)
+
+
+def test_next_row_entry_points_validation(lib):
+    """The fused write, the combine + projection / inverse RoPE and the window-run entry points
+    reject bad arguments before any device work."""
+    fake = ctypes.c_void_p(0x100000)
+    odd = ctypes.c_void_p(0x100004)
+    # mla_kv_write_norm_rope(raw, slots, positions, w, eps, freqs, max_pos, n, kv, layout, num_pages, ps, stream)
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 8, 0, None, 0, 4, 64, None) == 0
+    assert lib.mla_kv_write_norm_rope(fake, fake, None, fake, 1e-6, fake, 8, 4, fake, 0, 4, 64, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, -1.0, fake, 8, 4, fake, 0, 4, 64, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 0, 4, fake, 0, 4, 64, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, odd, 1e-6, fake, 8, 4, fake, 1, 4, 64, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 8, 4, fake, 5, 4, 64, None) == -1
+    # mla_combine_v_up(part_out, part_lse, ns, batch, sq, heads, sink, w, out, lse, o_v, status, stream)
+    assert lib.mla_combine_v_up(fake, fake, fake, 2, 1, 16, None, None, fake, fake, fake, None, None) == -1
+    assert lib.mla_combine_v_up(fake, None, fake, 2, 1, 16, None, fake, fake, fake, fake, None, None) == -1
+    assert lib.mla_combine_v_up(None, None, fake, 0, 1, 16, None, fake, fake, fake, fake, None, None) == -1
+    assert lib.mla_combine_v_up(None, None, fake, 2, 1, 16, None, odd, fake, fake, fake, None, None) == -1
+    # mla_combine_inv_rope(part_out, part_lse, ns, batch, sq, heads, sink, pos, freqs, max_pos, rope0, out, lse, s)
+    assert lib.mla_combine_inv_rope(None, None, fake, 2, 1, 64, None, fake, fake, 10, 450, fake, fake, None) == -1
+    assert lib.mla_combine_inv_rope(None, None, fake, 2, 1, 64, None, fake, fake, 10, 452, fake, fake, None) == -1
+    assert lib.mla_combine_inv_rope(None, None, fake, 2, 1, 64, None, None, fake, 10, 448, fake, fake, None) == -1
+    assert lib.mla_combine_inv_rope(None, None, fake, 2, 1, 64, None, fake, fake, 0, 448, fake, fake, None) == -1
+    # mla_swa_plan(kv_indices, lengths, T, topk, ps, step, runs, stream)
+    assert lib.mla_swa_plan(fake, None, 4, 128, 64, 2, fake, None) == -1
+    assert lib.mla_swa_plan(fake, None, 4, 128, 48, 1, fake, None) == -1
+    assert lib.mla_swa_plan(fake, None, 4, 128, 64, 1, odd, None) == -1
+    assert lib.mla_swa_plan(fake, None, 0, 128, 64, 1, fake, None) == -1
+    # mla_decode_runs(q, kv, layout, num_pages, ps, runs, window, batch, sq, heads, scale, sink, sched, ns,
+    #                 parts, splits, ws, ws_bytes, out, lse, flags, stream)
+    assert lib.mla_decode_runs(fake, fake, 1, 4, 64, None, 128, 2, 1, 64, 0.1, None, fake, fake, 1, 2, fake,
+                               1 << 20, fake, fake, 0, None) == -1
+    assert lib.mla_decode_runs(fake, fake, 1, 4, 64, odd, 128, 2, 1, 64, 0.1, None, fake, fake, 1, 2, fake,
+                               1 << 20, fake, fake, 0, None) == -1
+    assert lib.mla_decode_runs(fake, fake, 1, 4, 64, fake, 0, 2, 1, 64, 0.1, None, fake, fake, 1, 2, fake,
+                               1 << 20, fake, fake, 0, None) == -1
+    assert lib.mla_decode_runs(fake, fake, 1, 4, 64, fake, 128, 2, 2, 16, 0.1, None, fake, fake, 1, 2, fake,
+                               1 << 20, fake, fake, 0, None) == -2          # several tokens need heads % 64 == 0
