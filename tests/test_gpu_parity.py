@@ -386,6 +386,13 @@ SMALL = {
     "empty_bf16": lambda: workloads.dsv3(batch=4, seqlens=(0, 65, 0, 3), len_dist="fixed", new_rows=False),
     "heads20": lambda: workloads.dsv3(batch=2, heads=20, seqlens=(100, 700), len_dist="fixed"),
     "rows4096": lambda: workloads.verify(batch=1, sq=32, seqlens=(200,), len_dist="fixed"),
+    # a single head (one query row per token): M = 128 with one row used, Q boxes one row high
+    "heads1_bf16": lambda: workloads.dsv3(batch=3, heads=1, seqlens=(1, 77, 1300), len_dist="fixed"),
+    "heads1_fp8_sink": lambda: workloads.dsv4(batch=3, heads=1, seqlens=(2, 65, 900), len_dist="fixed"),
+    # two draft tokens x 64 heads: 128 rows = two query groups, each one token, causal
+    "verify_sq2_h64": lambda: workloads.verify(batch=3, sq=2, heads=64, seqlens=(3, 130, 900), len_dist="fixed"),
+    # draft tokens with fp8 rows and a sink
+    "verify_fp8_sink": lambda: workloads.dsv4(batch=2, sq=3, seqlens=(40, 500), len_dist="fixed", causal=True),
 }
 
 
