@@ -187,23 +187,54 @@ __device__ __forceinline__ void write_row(const uint16_t* x, int lane, uint8_t* 
   const int nope = layout == 1 ? 448 : 512;
   const int row_bytes = layout == 1 ? 576 : 640;
   uint8_t* dst = kv + page * page_bytes + (int64_t)off * row_bytes;
-  uint32_t sbytes[2] = {0u, 0u};
-  for (int g = 0; g < nope / 64; ++g) {
-    const uint32_t two = *reinterpret_cast<const uint32_t*>(x + g * 64 + 2 * lane);
-    const float x0 = bf16_to_f32(two & 0xFFFFu), x1 = bf16_to_f32(two >> 16);
-    float a = fmaxf(fabsf(x0), fabsf(x1));
+  // lane l holds elements [16 l, 16 l + 16), loaded at once; NoPE group g is lanes 4g .. 4g+3
+  // (in the 512-wide DSV4 row, lanes 28-31 hold the RoPE part)
+  float v[16];
+  {
+    const uint4 a = reinterpret_cast<const uint4*>(x)[2 * lane];
+    const uint4 b = reinterpret_cast<const uint4*>(x)[2 * lane + 1];
+    const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    a = fmaxf(a, 1e-10f);
-    const int e = group_exponent(a);
-    const float sc = pow2neg(e);
-    uint16_t codes;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(codes) : "f"(x1 * sc), "f"(x0 * sc));
-    *reinterpret_cast<uint16_t*>(dst + g * 64 + 2 * lane) = codes;
-    sbytes[g >> 2] |= static_cast<uint32_t>(e + 127) << (8 * (g & 3));
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = bf16_to_f32(h[k] & 0xFFFFu);
+      v[2 * k + 1] = bf16_to_f32(h[k] >> 16);
+    }
   }
-  // RoPE part: 64 bf16 copied
-  if (lane < 8)
+  const bool in_nope = lane * 16 < nope;
+  float a = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(v[k]));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  a = fmaxf(a, 1e-10f);
+  const int e = group_exponent(a);
+  if (in_nope) {
+    const float sc = pow2neg(e);
+    uint32_t w4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint16_t c0, c1;
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c0) : "f"(v[4 * k + 1] * sc), "f"(v[4 * k] * sc));
+      asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c1) : "f"(v[4 * k + 3] * sc), "f"(v[4 * k + 2] * sc));
+      w4[k] = static_cast<uint32_t>(c0) | (static_cast<uint32_t>(c1) << 16);
+    }
+    reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  } else {
+    // DSV4 row: its 64 RoPE elements stay bf16, after the 448 code bytes
+    const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * lane;
+    uint4* d2 = reinterpret_cast<uint4*>(dst + nope + (lane * 16 - nope) * 2);
+    d2[0] = src[0];
+    d2[1] = src[1];
+  }
+  // scale bytes: group g's exponent sits in lane 4g; lane 0 assembles the 8-byte slot
+  uint32_t sbytes[2] = {0u, 0u};
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const int eg = __shfl_sync(0xffffffffu, e, 4 * g);
+    if (g < nope / 64) sbytes[g >> 2] |= static_cast<uint32_t>(eg + 127) << (8 * (g & 3));
+  }
+  // the 576-wide row's RoPE part: 64 bf16 copied
+  if (layout != 1 && lane < 8)
     reinterpret_cast<uint4*>(dst + nope)[lane] = reinterpret_cast<const uint4*>(x + nope)[lane];
   if (lane == 0) {
     uint2* sp = reinterpret_cast<uint2*>(kv + page * page_bytes + (int64_t)page_size * row_bytes + off * 8);
