@@ -252,8 +252,9 @@ int mla_combine(const float* part_out, const float* part_lse, const int32_t* num
  * mapped to its head's value space, o_v = x W_UV[n] ("mla_attention.py ·
  * tduncan/Nvidia-Optimization-Stack-VLLM": _v_up_proj multiplies the (N, B, L)
  * latent output by W_UV (N, L, V)).
- *  part_out, part_lse, num_splits, sink: as for mla_combine (part_out and part_lse
- *         may be NULL when no request has two or more splits).
+ *  part_out, part_lse, num_splits, sink: as for mla_combine. part_out and part_lse
+ *         may be NULL (both): then no row is merged and every row of out is taken as
+ *         written (for a plan in which no request has two or more splits).
  *  w_uv   device bf16 [num_heads, 512, 128] (value head dim 128), 16-byte aligned.
  *  out    device bf16 [T, N, 512]: read for requests with one split (the decode
  *         wrote it); for split requests the merged row is written here first,
@@ -273,8 +274,8 @@ int mla_combine_v_up(const float* part_out, const float* part_lse, const int32_t
  * 448 NoPE + 64 RoPE, O "before the inverse RoPE"; "MLA" API page of HALOps,
  * mla_output_proj: "the split-KV LSE combine and inverse RoPE of O").
  * Every row of out [T, N, 512] (bf16, in place) is first merged as mla_combine
- * merges it when its request has two or more splits (writing lse too), or taken as
- * the decode wrote it; then elements [rope0, rope0 + 64) are rotated back: pair i =
+ * merges it when its request has two or more splits and part_out / part_lse are
+ * given (writing lse too), or taken as the decode wrote it; then elements [rope0, rope0 + 64) are rotated back: pair i =
  * (u, v) -> (u c + v s, v c - u s) with (c, s) = freqs[positions[t], 2i .. 2i + 1],
  * in fp32, and rounded to bf16. Rows of a token whose position is outside
  * [0, max_pos) are merged but not rotated.

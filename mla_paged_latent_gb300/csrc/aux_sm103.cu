@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) combine_inv_rope_kernel(
   const int s0 = num_splits[b];
   const int ns = num_splits[b + 1] - s0;
   float acc[16];
-  if (ns >= 2) {
+  if (ns >= 2 && part_out != nullptr) {  // no partials given: every row is taken as written
     const float lse_tot = merge_row(part_out, part_lse, s0, ns, R, row, lane, sink, row % heads, acc);
     store_row_bf16(out + orow * 512, lane, acc);  // acc now holds the bf16 values
     if (lane == 0) lse[orow] = lse_tot;

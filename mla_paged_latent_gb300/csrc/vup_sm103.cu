@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kVupThreads, 1)
         const int row = (t % P.sq) * P.heads + n;
         const int s0 = P.num_splits[b];
         const int ns = P.num_splits[b + 1] - s0;
-        if (ns >= 2) {
+        if (ns >= 2 && P.part_out != nullptr) {
           for (int s = 0; s < ns; ++s)
             prefetch_l2_bulk(P.part_out + ((int64_t)(s0 + s) * R + row) * 512, 2048);
         } else {
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kVupThreads, 1)
         const int64_t orow = (int64_t)b * R + row;
         const int s0 = P.num_splits[b];
         const int ns = P.num_splits[b + 1] - s0;
-        if (ns >= 2) {
+        if (ns >= 2 && P.part_out != nullptr) {
           // merged exactly as the combine kernel merges it, and written back the same way
           const float lse_tot = merge_row(P.part_out, P.part_lse, s0, ns, R, row, lane, P.sink, n, acc);
           store_row_bf16(P.out + orow * 512, lane, acc);

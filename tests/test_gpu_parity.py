@@ -240,6 +240,35 @@ def test_combine_v_up_matches_oracle(B, sq, N, splits):
     assert np.all(excess <= 0), f"o_v: worst excess {excess.max():.3g} at {np.unravel_index(np.argmax(excess), excess.shape)}"
 
 
+def test_combine_steps_without_partials_take_rows_as_written():
+    """With no partials given, the combine + projection and combine + inverse RoPE take every
+    row of out as written, even where num_splits counts several splits (nothing is merged)."""
+    rng = np.random.default_rng(99)
+    B, N = 4, 64
+    T = B
+    ns = torch.tensor([0, 3, 4, 6, 7], dtype=torch.int32, device="cuda")   # splits, but no partials
+    out_bits = torch.from_numpy(rng.standard_normal((T, N, 512)).astype(np.float32)).to(torch.bfloat16)
+    out_bits = out_bits.view(torch.int16).numpy().view(np.uint16)
+    w_bits = torch.from_numpy((rng.standard_normal((N, 512, 128)) * 0.05).astype(np.float32)).to(torch.bfloat16)
+    w_bits = w_bits.view(torch.int16).numpy().view(np.uint16)
+    out = torch.from_numpy(out_bits.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    lse = torch.zeros(T, N, dtype=torch.float32, device="cuda")
+    o_v = torch.zeros(T, N, 128, dtype=torch.bfloat16, device="cuda")
+    mla.mla_combine_v_up(None, None, ns, 1, N, bf16_tensor(w_bits), out, lse, o_v)
+    freqs = _rope_table(16)
+    mla.mla_combine_inv_rope(None, None, ns, 1, N, torch.zeros(T, dtype=torch.int32, device="cuda"),
+                             torch.from_numpy(freqs).cuda(), out, lse, rope0=448)
+    torch.cuda.synchronize()
+    # position 0: angle 0, the rotation is the identity
+    assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), out_bits)
+    ref = _bits_to_f64(oracle.v_up(out_bits, w_bits))
+    got = o_v.float().cpu().numpy().astype(np.float64)
+    x_abs = np.abs(_bits_to_f64(out_bits))
+    w_abs = np.abs(_bits_to_f64(w_bits))
+    tol = np.abs(ref) * 2.0 ** -8 + np.einsum("tnl,nlv->tnv", x_abs, w_abs) * 1e-4
+    assert np.all(np.abs(got - ref) <= tol)
+
+
 @pytest.mark.parametrize("B,sq,N,splits", [(3, 2, 64, (3, 1, 5)), (8, 1, 64, None)])
 def test_combine_inv_rope_matches_oracle(B, sq, N, splits):
     """Split combine + inverse RoPE of elements 448..511 (the DSV4 value row) against the
