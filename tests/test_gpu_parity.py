@@ -490,6 +490,56 @@ def test_large_score_growth_triggers_rescale():
     assert_close(out, lse, ref_out, ref_lse, "rescale")
 
 
+def _scale_rope_with_position(w, row_bytes, nope_bytes, growth):
+    """Multiply the bf16 RoPE part of every valid KV row j by (1 + j/growth), in place."""
+    ps = w.cfg.page_size
+    kv = w.kv_cache.copy()
+    for b in range(w.seqlens.shape[0]):
+        for j in range(int(w.seqlens[b])):
+            page = w.block_table[b, j // ps]
+            off = (j % ps) * row_bytes + nope_bytes
+            rope = kv[page, off:off + 128].view(np.int16).copy()
+            vals = torch.from_numpy(rope).view(torch.bfloat16).float() * (1 + j / growth)
+            kv[page, off:off + 128] = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint8)
+    w.kv_cache = kv
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_fp8_score_growth_triggers_rescale(layout):
+    """fp8 layouts: scores that grow along the sequence (RoPE part of row j scaled by
+    1 + j/8, q's RoPE part 2; ~120 in log2 units at the end) raise the running max
+    past the 2^32 lazy-rescale threshold several times per query row, so O is
+    rescaled in TMEM between tiles. In the 448 layout V includes the RoPE part
+    (|V| up to ~450), which the bf16 pair P_hi + P_lo carries within the bound."""
+    cfg = workloads.dsv4(batch=2, heads=64, seqlens=(640, 1000), len_dist="fixed", new_rows=False, sink=False,
+                         layout=layout)
+    w = workloads.generate(cfg)
+    _scale_rope_with_position(w, 576 if layout == 1 else 640, 448 if layout == 1 else 512, 8)
+    w.q[:, :, -64:] = torch.full((1,), 2.0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)[0]
+    d = DeviceWorkload(w)
+    out, lse = d.run()
+    ref_out, ref_lse = oracle_decode(w)
+    assert_close(out, lse, ref_out, ref_lse, f"fp8 rescale layout {layout}")
+
+
+def test_large_query_value():
+    """One q element of 1e5 (bf16 holds it): that head's scores are ~1e4 apart, its
+    softmax picks one row and its lse is ~1e4, compared relatively since fp32 carries
+    it to a few ulps (~2e-3 each); every other head is unaffected."""
+    cfg = workloads.dsv3(batch=2, heads=64, seqlens=(100, 70), len_dist="fixed", new_rows=False)
+    w = workloads.generate(cfg)
+    w.q[1, 3, 20] = np.uint16(torch.tensor([1.0e5]).to(torch.bfloat16).view(torch.int16).item() & 0xFFFF)
+    d = DeviceWorkload(w)
+    out, lse = d.run()   # asserts a zero status word
+    ref_out, ref_lse = oracle_decode(w)
+    keep = np.ones(lse.shape, dtype=bool)
+    keep[1, 3] = False
+    assert_close(out[keep], lse[keep], ref_out[keep], ref_lse[keep], "bf16 large q, other heads")
+    assert_close(out[1, 3][None], np.zeros(1), ref_out[1, 3][None], np.zeros(1), "bf16 large q, that head's output")
+    # the score's fp32 sum of terms ~1e4 is good to a few of its ulps (~2e-3 each)
+    assert abs(lse[1, 3] - ref_lse[1, 3]) <= 1e-5 * abs(ref_lse[1, 3])
+
+
 def test_causal_with_short_context():
     """Draft tokens whose visible prefix is empty (L < s_q) give zero output and -inf lse."""
     cfg = workloads.verify(batch=2, heads=64, seqlens=(2, 6), len_dist="fixed")
