@@ -422,6 +422,12 @@ SMALL = {
     "verify_sq2_h64": lambda: workloads.verify(batch=3, sq=2, heads=64, seqlens=(3, 130, 900), len_dist="fixed"),
     # draft tokens with fp8 rows and a sink
     "verify_fp8_sink": lambda: workloads.dsv4(batch=2, sq=3, seqlens=(40, 500), len_dist="fixed", causal=True),
+    # top-k lists mostly padding (-1): 3 of 10 tiles hold rows, so split units start on, or
+    # consist only of, tiles with no valid row; and lists that are padding throughout
+    "sparse_padded": lambda: workloads.sparse(batch=3, seqlens=(5000, 300, 7000), topk=640, pad_frac=0.7,
+                                              len_dist="fixed"),
+    "sparse_all_pad": lambda: workloads.sparse(batch=2, seqlens=(900, 4000), topk=256, pad_frac=1.0,
+                                               len_dist="fixed"),
 }
 
 
@@ -436,7 +442,7 @@ def test_decode_small(name):
     assert_close(out, lse, ref_out, ref_lse, name)
 
 
-@pytest.mark.parametrize("name", ["dsv3_small", "dsv4_small", "verify_small", "sparse_small"])
+@pytest.mark.parametrize("name", ["dsv3_small", "dsv4_small", "verify_small", "sparse_small", "sparse_padded"])
 @pytest.mark.parametrize("num_sms", [1, 7, 40])
 def test_decode_forced_splits(name, num_sms):
     """Few partitions -> long partitions; many partitions -> many splits merged
