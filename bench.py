@@ -603,21 +603,25 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        t0 = time.perf_counter()
-        kv_o = oracle.kv_write(w.new_rows, w.new_slots, w.kv_cache, c.layout, c.page_size) \
-            if w.new_rows is not None else w.kv_cache
         if args.config in ("dsv3", "tiny", "dsv4"):
             toks = np.arange(T)
         else:
             toks = np.arange(min(T, 32))
         sel_t = np.repeat(toks, N).astype(np.int32)
         sel_n = np.tile(np.arange(N), len(toks)).astype(np.int32)
-        oracle.mla_decode(w.q, kv_o, c.layout, c.page_size, w.block_table, w.seqlens, c.sq, c.sm_scale, sink=w.sink,
-                          indices=w.indices, causal=c.causal, select=(sel_t, sel_n))
-        dt = time.perf_counter() - t0
-        cpu = {"value": len(toks) / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+        # whole passes (kv_write + decode of the sampled tokens) until about 10 s of CPU work
+        t0 = time.perf_counter()
+        passes, dt = 0, 0.0
+        while passes == 0 or (dt < 10.0 and passes < 8):
+            kv_o = oracle.kv_write(w.new_rows, w.new_slots, w.kv_cache, c.layout, c.page_size) \
+                if w.new_rows is not None else w.kv_cache
+            oracle.mla_decode(w.q, kv_o, c.layout, c.page_size, w.block_table, w.seqlens, c.sq, c.sm_scale,
+                              sink=w.sink, indices=w.indices, causal=c.causal, select=(sel_t, sel_n))
+            passes += 1
+            dt = time.perf_counter() - t0
+        cpu = {"value": passes * len(toks) / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{len(toks)} query tokens x {N} heads of the {args.config} batch (+ its kv_write), "
-                         f"fp64 C oracle, OpenMP over tokens, {dt:.1f} s"}
+                         f"{passes} pass(es), fp64 C oracle, OpenMP over tokens, {dt:.1f} s"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
