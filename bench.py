@@ -49,9 +49,9 @@ def load_peaks():
 
 
 def algorithmic_cost(w):
-    """Bytes and MMA FLOPs one decode launch must move / perform (per the scope
-    table): every candidate KV row once (row + its scale slot for fp8), q, out,
-    lse (and the sparse index list)."""
+    """Bytes and MMA FLOPs one decode launch must move / perform: every candidate
+    KV row once (row + its scale slot for fp8), q, out, lse (and the sparse index
+    list); 2 x (D_qk + 512) FLOPs per candidate row and query row."""
     c = w.cfg
     T, N = w.q.shape[0], c.heads
     row_b = {0: 1152, 1: 576 + 8, 2: 640 + 8}[c.layout]
