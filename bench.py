@@ -133,13 +133,40 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def _code_tokens(text):
+    """C / C++ / CUDA source with its comments removed and every run of whitespace
+    made one space (string and character literals kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash():
+    """Hash of the library's code (csrc, comments and layout of whitespace aside): the
+    recorded ncu counters stay valid while it is unchanged."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mla_paged_latent_gb300", "csrc")
     for name in sorted(os.listdir(d)):
-        with open(os.path.join(d, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(d, name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

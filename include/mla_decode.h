@@ -271,8 +271,8 @@ int mla_combine_v_up(const float* part_out, const float* part_lse, const int32_t
 /*
  * Split combine fused with the inverse RoPE of the output (device): the step after
  * the decode for rows whose value part carries RoPE (the DSV4 row: value dim 512 =
- * 448 NoPE + 64 RoPE, O "before the inverse RoPE"; "MLA" API page of HALOps,
- * mla_output_proj: "the split-KV LSE combine and inverse RoPE of O").
+ * 448 NoPE + 64 RoPE, whose O still carries the rotation; "MLA" API page of HALOps,
+ * mla_output_proj, which merges the split-KV partials by LSE and then undoes the RoPE).
  * Every row of out [T, N, 512] (bf16, in place) is first merged as mla_combine
  * merges it when its request has two or more splits and part_out / part_lse are
  * given (writing lse too), or taken as the decode wrote it; then elements [rope0, rope0 + 64) are rotated back: pair i =
@@ -288,7 +288,7 @@ int mla_combine_inv_rope(const float* part_out, const float* part_lse, const int
 
 /*
  * KV-row write (device): scatter n new rows into their pages ("MLA" API page of
- * HALOps, mla_attention: "RMSNorm + RoPE + KV cache write"; kv_cache parameter).
+ * HALOps, mla_attention: its cache-write step and kv_cache parameter).
  *  rows   device bf16 [n, row_elems], already RMSNorm'd (and RoPE'd);
  *         row_elems = 576 (layouts 0 and 2) or 512 (layout 1: 448 NoPE | 64 RoPE).
  *  slots  device int32 [n]: page * page_size + offset; negative slots are skipped.
@@ -303,8 +303,8 @@ int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cac
 /*
  * Normalise, rotate and write new KV rows (device): the step that produces a
  * cache row from the latent projection, fused with mla_kv_write ("MLA" API page
- * of HALOps, mla_attention: "q / kv RMSNorm + RoPE + KV cache write"; its
- * kv_norm_weight, kv_eps, positions and freqs_real parameters).
+ * of HALOps, mla_attention: the step that normalises and rotates q and kv before the
+ * cache write; its kv_norm_weight, kv_eps, positions and freqs_real parameters).
  *  raw     device bf16 [n, row_elems], the un-normalised rows; row_elems = 576
  *          for layouts 0 and 2 ([kv_c 512 | k_pe 64]) and 512 for layout 1 (the
  *          DSV4 row: 448 NoPE | 64 RoPE).

@@ -41,7 +41,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // One warp per query row: the merged (split) or decode-written (unsplit) row, with the
 // inverse RoPE applied to elements [rope0, rope0 + 64): pair i = (u, v) -> (u c + v s,
 // v c - u s), (c, s) = freqs[pos, 2i], freqs[pos, 2i + 1] ("MLA" API page of HALOps,
-// mla_output_proj: "the split-KV LSE combine and inverse RoPE of O"). Written back to out.
+// mla_output_proj: the split-KV partials merged by LSE, then the RoPE of O undone). Written
+// back to out.
 __global__ void __launch_bounds__(256) combine_inv_rope_kernel(
     const float* __restrict__ part_out, const float* __restrict__ part_lse, const int32_t* __restrict__ num_splits,
     int R, int sq, int heads, const float* __restrict__ sink, const int32_t* __restrict__ positions,
@@ -262,8 +263,8 @@ __global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restric
 }
 
 // One warp per raw row: RMSNorm of the 512 latent elements and RoPE of the 64 RoPE
-// elements in fp32 ("MLA" API page of HALOps, mla_attention: "q / kv RMSNorm + RoPE
-// + KV cache write", kv_norm_weight / kv_eps / positions / freqs_real), the row
+// elements in fp32 ("MLA" API page of HALOps, mla_attention: its normalise-and-rotate
+// step before the cache write, kv_norm_weight / kv_eps / positions / freqs_real), the row
 // rounded to bf16 in shared memory, then written as write_row writes it. Lane l
 // holds latent elements [16 l, 16 l + 16) and RoPE pair l of the 576-wide layouts.
 __global__ void __launch_bounds__(128) kv_write_norm_rope_kernel(

@@ -26,8 +26,8 @@
  *              softmax denominator), and the supported-config paragraph (one
  *              ue8m0 scale per 64 NoPE elements, value dim 512).
  *              The same entry's kv_norm_weight, kv_eps, positions and freqs_real
- *              parameters and its "q / kv RMSNorm + RoPE + KV cache write" step
- *              define mo_kv_norm_rope.
+ *              parameters and its step that normalises and rotates the kv row
+ *              before the cache write define mo_kv_norm_rope.
  *  [sglang-FlashMLA] "Implementation:Sgl project Sglang Flash MLA", I/O Contract
  *              (q, k_cache, block_table, cache_seqlens, softmax_scale, causal,
  *              indices -> out, softmax_lse).
@@ -467,8 +467,8 @@ void mo_v_up(const uint16_t* x, const uint16_t* w, int T, int N, int dv, uint16_
       }
 }
 
-/* Inverse RoPE of attention output rows ([HALOps-MLA] mla_output_proj: "inverse RoPE
- * of O"): for each bf16 row [512], elements [rope0, rope0 + 64) hold 32 interleaved
+/* Inverse RoPE of attention output rows ([HALOps-MLA] mla_output_proj, which undoes
+ * the rotation of O): for each bf16 row [512], elements [rope0, rope0 + 64) hold 32 interleaved
  * pairs (u, v) rotated by the position's angle; they are rotated back,
  * (u, v) -> (u c + v s, v c - u s) with (c, s) = freqs[pos, 2i], freqs[pos, 2i+1],
  * and rounded to bf16. Rows with a position outside [0, max_pos) are copied. */
