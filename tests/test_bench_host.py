@@ -23,3 +23,34 @@ def test_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     assert bench.source_hash() == h0
     p.write_text(text.replace("acc[i] *= f;", "acc[i] *= 2.f * f;", 1))
     assert bench.source_hash() != h0
+
+
+def test_algorithmic_cost_tiny_closed_form():
+    """The roofline numerator on the tiny workload (2 requests of 37 and 130 rows, 16
+    heads, bf16 rows of 1152 B): every KV row once, q, out and lse; 2 x (576 + 512)
+    FLOPs per (row, query row)."""
+    import workloads
+    w = workloads.generate(workloads.tiny())
+    c = bench.algorithmic_cost(w)
+    T, N = 2, 16
+    assert c["kv_rows"] == 37 + 130
+    assert c["kv_bytes"] == 167 * 1152
+    assert c["bytes"] == 167 * 1152 + T * N * 576 * 2 + T * N * 512 * 2 + T * N * 4
+    assert c["flops"] == 2.0 * 167 * N * (576 + 512)
+
+
+def test_algorithmic_cost_causal_and_sparse_by_brute_force():
+    """Causal verify counts, per draft token i, the rows j <= L - s_q + i; sparse counts
+    the valid listed entries (0 <= idx < L) once per token."""
+    import numpy as np
+    import workloads
+    w = workloads.generate(workloads.verify(batch=3, sq=4, heads=16, seqlens=(2, 9, 70), len_dist="fixed"))
+    scored = sum(sum(1 for j in range(L) if j <= L - 4 + i) for L in (2, 9, 70) for i in range(4))
+    assert bench.algorithmic_cost(w)["flops"] == 2.0 * scored * 16 * (576 + 512)
+    w = workloads.generate(workloads.sparse(batch=2, seqlens=(900, 4000), topk=256, len_dist="fixed"))
+    valid = sum(int(((w.indices[t] >= 0) & (w.indices[t] < w.seqlens[t])).sum()) for t in range(2))
+    c = bench.algorithmic_cost(w)
+    assert c["kv_rows"] == valid
+    assert c["kv_bytes"] == valid * (640 + 8)
+    assert c["flops"] == 2.0 * valid * 128 * (576 + 512)
+    assert c["bytes"] == valid * 648 + 2 * 128 * 576 * 2 + 2 * 128 * 512 * 2 + 2 * 128 * 4 + w.indices.nbytes
