@@ -127,6 +127,34 @@ def test_fp8_page_layout_golden(oracle_lib):
     assert np.array_equal(oracle.decode_row(page, oracle.LAYOUT_FP8_448, 2, 0, 0), np.zeros(512))
 
 
+def test_fp8_512_page_layout_golden(oracle_lib):
+    """The fp8-512 page (640-B rows, 8 ue8m0 bytes per scale slot) from a hand-built
+    fixture: row stride, scale-slot offset, the eighth group's scale and the RoPE
+    offset 512 are each exercised by one nonzero value."""
+    ent = _read_fixture("fp8_512_page_ps2.txt")
+    pb = int([e for e in ent if e[0] == "page_bytes"][0][1])
+    info = oracle.layout_info(oracle.LAYOUT_FP8_512, 2)
+    assert info["page_bytes"] == pb and info["dqk"] == 576 and info["row_bytes"] == 640
+    page = np.zeros((1, pb), dtype=np.uint8)
+    for e in ent:
+        if e[0] in ("row0_nope", "row1_nope"):
+            page[0, 640 * int(e[0][3]) + int(e[1])] = int(e[2], 0)
+        elif e[0] in ("row0_scale", "row1_scale"):
+            page[0, 2 * 640 + 8 * int(e[0][3]) + int(e[1])] = int(e[2], 0)
+        elif e[0] == "row1_rope":
+            v = int(e[2], 0)
+            o = 640 + 512 + 2 * int(e[1])
+            page[0, o], page[0, o + 1] = v & 0xFF, v >> 8
+    expect0, expect1 = np.zeros(576), np.zeros(576)
+    for e in ent:
+        if e[0] == "expect0":
+            expect0[int(e[1])] = float(e[2])
+        elif e[0] == "expect":
+            expect1[int(e[1])] = float(e[2])
+    assert np.array_equal(oracle.decode_row(page, oracle.LAYOUT_FP8_512, 2, 0, 0), expect0)
+    assert np.array_equal(oracle.decode_row(page, oracle.LAYOUT_FP8_512, 2, 0, 1), expect1)
+
+
 def test_page_sizes(oracle_lib):
     # page_bytes a multiple of the row size ("MLA" API page of HALOps, kv_cache parameter)
     assert oracle.layout_info(0, 64)["page_bytes"] == 64 * 1152
@@ -279,6 +307,59 @@ def test_verify_causal_matches_torch_sdpa(oracle_lib):
     assert np.allclose(lse, rl, atol=1e-12)
 
 
+def _torch_fp8_rows(kv_cache, layout, ps, bt_row, pos):
+    """KV rows at request positions `pos`, decoded with torch's float8_e4m3fn and bfloat16
+    conversions from bytes cut out of the pages by plain slicing: a page holds ps rows of
+    (nope e4m3 | 64 bf16) followed by ps 8-byte slots of ue8m0 scale bytes, one per 64
+    NoPE elements ("MLA" API page of HALOps, mla_attention, kv_cache parameter and the
+    supported-config paragraph)."""
+    nope = {1: 448, 2: 512}[layout]
+    rb = nope + 128
+    pos = np.asarray(pos, dtype=np.int64)
+    pg = np.asarray(bt_row, dtype=np.int64)[pos // ps]
+    off = pos % ps
+    rows = kv_cache[pg[:, None], off[:, None] * rb + np.arange(rb)[None, :]]
+    slots = kv_cache[pg[:, None], ps * rb + off[:, None] * 8 + np.arange(8)[None, :]]
+    codes = torch.from_numpy(np.ascontiguousarray(rows[:, :nope])).view(torch.float8_e4m3fn).double()
+    scale = torch.from_numpy(np.ascontiguousarray(slots[:, :nope // 64])).view(torch.float8_e8m0fnu).double()
+    k_nope = codes * scale.repeat_interleave(64, dim=1)
+    rope = torch.from_numpy(np.ascontiguousarray(rows[:, nope:]).view(np.int16)).view(torch.bfloat16).double()
+    return torch.cat([k_nope, rope], dim=1)
+
+
+@pytest.mark.parametrize("layout,sparse", [(1, False), (2, False), (2, True)])
+def test_fp8_decode_matches_torch_sdpa(oracle_lib, layout, sparse):
+    """Both fp8 layouts, dense and top-k: the oracle's paged decode against torch float64
+    SDPA over rows decoded by torch's own fp8 / e8m0 / bf16 conversions. V is the first
+    512 elements of the decoded row: kv_c for the 576-wide row, the whole row (448 NoPE +
+    64 RoPE) for the 512-wide one."""
+    if sparse:
+        cfg = workloads.sparse(batch=2, heads=8, seqlens=(300, 1000), topk=96, pad_frac=0.25, page_size=16)
+    elif layout == 1:
+        cfg = workloads.dsv4(batch=2, heads=8, seqlens=(70, 300), len_dist="fixed", page_size=16, sink=False)
+    else:
+        cfg = workloads.sparse(batch=2, heads=8, seqlens=(70, 300), topk=0, min_splits=1, page_size=16)
+    w = workloads.generate(cfg)
+    out, lse = oracle.mla_decode(w.q, w.kv_cache, layout, 16, w.block_table, w.seqlens, 1, cfg.sm_scale,
+                                 indices=w.indices)
+    q = torch.from_numpy(w.q.view(np.int16).copy()).view(torch.bfloat16).double()
+    for t in range(cfg.batch):
+        L = int(w.seqlens[t])
+        if sparse:
+            pos = [int(i) for i in w.indices[t] if 0 <= i < L]
+        else:
+            pos = list(range(L))
+        K = _torch_fp8_rows(w.kv_cache, layout, 16, w.block_table[t], pos)
+        assert K.shape[1] == q.shape[2]
+        N = q.shape[1]
+        ro = torch.nn.functional.scaled_dot_product_attention(q[t][:, None], K[None].expand(N, -1, -1),
+                                                              K[None, :, :512].expand(N, -1, -1),
+                                                              scale=cfg.sm_scale)[:, 0]
+        rl = torch.logsumexp((q[t] @ K.T) * cfg.sm_scale, dim=1)
+        assert np.allclose(out[t], ro.numpy(), rtol=0, atol=1e-11)
+        assert np.allclose(lse[t], rl.numpy(), rtol=0, atol=1e-11)
+
+
 def test_causal_reductions(oracle_lib):
     """Causal verify (bottom-right, seq_len = context_len + query_len,
     "mla_attention.py", MLACommonMetadata): s_q = 1 equals dense; token i equals
@@ -413,22 +494,29 @@ def test_kv_write_bf16_is_bit_copy(oracle_lib):
         assert np.array_equal(out[p, o * 1152:(o + 1) * 1152].view(np.uint16), bits[r])
 
 
-def test_kv_write_then_decode_roundtrip_error(oracle_lib):
-    rng = np.random.default_rng(11)
-    x = rng.standard_normal((8, 512)).astype(np.float32)
+@pytest.mark.parametrize("layout", [1, 2])
+def test_kv_write_then_decode_roundtrip_error(oracle_lib, layout):
+    """Write then read back, both fp8 layouts: every NoPE element within half an E4M3
+    step of its input (relative 2^-4 for normals, absolute 2^(e-10) below), the RoPE
+    elements bit-exact, on rows whose groups span 2^-20 .. 2^20 in magnitude."""
+    nope = {1: 448, 2: 512}[layout]
+    rng = np.random.default_rng(11 + layout)
+    group_scale = np.repeat(2.0 ** rng.integers(-20, 21, (8, (nope + 64) // 64)), 64, axis=1)
+    x = (rng.standard_normal((8, nope + 64)) * group_scale).astype(np.float32)
     bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     xb = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
-    kv = oracle.kv_write(bits, np.arange(8, dtype=np.int32), np.zeros((1, oracle.layout_info(1, 8)["page_bytes"]),
-                                                                      np.uint8), 1, 8)
+    kv = oracle.kv_write(bits, np.arange(8, dtype=np.int32),
+                         np.zeros((1, oracle.layout_info(layout, 8)["page_bytes"]), np.uint8), layout, 8)
     for r in range(8):
-        k = oracle.decode_row(kv, 1, 8, 0, r)
-        for g in range(7):
+        k = oracle.decode_row(kv, layout, 8, 0, r)
+        assert k.shape == (nope + 64,)
+        for g in range(nope // 64):
             grp = xb[r, g * 64:(g + 1) * 64]
             e = oracle.group_exponent(max(np.abs(grp).max(), 1e-10))
             # E4M3 relative half-ulp is 2^-4 for normals; absolute floor 2^-10 (half subnormal step) * 2^e
             err = np.abs(k[g * 64:(g + 1) * 64] - grp)
             assert np.all(err <= np.maximum(np.abs(grp) * 2.0 ** -4, 2.0 ** (e - 10)) + 1e-300)
-        assert np.array_equal(k[448:], xb[r, 448:])
+        assert np.array_equal(k[nope:], xb[r, nope:])
 
 
 def test_kv_gather_matches_decode_row(oracle_lib):
