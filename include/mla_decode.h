@@ -61,6 +61,8 @@ extern "C" {
 /* Bits of the device status word (mla_read_status). */
 #define MLA_STATUS_WAIT_TIMEOUT 1u        /* a pipeline wait gave up after ~2 s */
 #define MLA_STATUS_BAD_PAGE 2u            /* a block_table entry needed for a row < L is outside [0, num_pages) */
+#define MLA_STATUS_BAD_SLOT 4u            /* a KV write slot's page is outside [0, num_pages): row not written */
+#define MLA_STATUS_BAD_POSITION 8u        /* a fused write's position is outside [0, max_pos): row not written */
 
 typedef enum {
   MLA_KV_BF16_576 = 0,
@@ -74,6 +76,10 @@ typedef enum {
 #define MLA_GROUP_ROWS 64       /* query rows (token x head) per CTA work item */
 #define MLA_WORKSPACE_HEADER 256
 #define MLA_DECODE_SKIP_COMBINE 1u  /* mla_decode flag: leave split partials in the workspace */
+/* mla_decode flag: run a bf16 decode whose query rows come in groups of 128 (for example
+ * 128 heads) on the CTA-pair kernel, two SMs per group of 128 query rows, instead of the
+ * single-SM kernel (same results within the stated tolerances). Ignored for other decodes. */
+#define MLA_DECODE_CTA_PAIR 2u
 /* mla_decode flag, for testing failure detection only: the decode kernel withholds
  * the signal that its first score tile is complete, so the softmax's bounded wait
  * runs out; every role then leaves its loop, the call completes, and the workspace
@@ -162,7 +168,8 @@ int mla_decode_plan(const int32_t* cache_seqlens, int32_t batch, int32_t q_token
  * flags has MLA_DECODE_SKIP_COMBINE, in which case the caller runs mla_combine
  * on the workspace partials (layout: MLA_WORKSPACE_HEADER bytes of status, then
  * part_lse float [total_splits, R] padded to a multiple of 256 bytes, then
- * part_out float [total_splits, R, 512], R = q_tokens_per_req * num_heads).
+ * part_out float [total_splits, R, 512], R = q_tokens_per_req * num_heads, then the
+ * partial max logits of mla_sparse_prefill, float [total_splits, R] padded to 256 bytes).
  */
 int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages, int32_t page_size,
                const int32_t* block_table, int32_t max_pages, const int32_t* cache_seqlens, int32_t batch,
@@ -170,6 +177,32 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
                const int32_t* indices, int32_t topk, int32_t causal, const int32_t* sched,
                const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
                size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream);
+
+/*
+ * Sparse prefill (device): "Implementation:Sgl project Sglang Flash MLA", Signature and
+ * I/O Contract of flash_mla_sparse_fwd (q, kv, indices, sm_scale, d_v = 512 -> out,
+ * max_logits, lse). Every token attends over its own top-k list of rows of one unpaged
+ * latent run.
+ *  q        device bf16 [num_tokens, num_heads, 576] (16-B aligned).
+ *  kv       device bf16 [s_kv, 576]: the latent rows [kv_c 512 | k_pe 64] (16-B aligned);
+ *           K = row, V = row[0:512].
+ *  indices  device int32 [num_tokens, topk]: positions in kv; entries outside
+ *           [0, s_kv) are skipped, duplicates count twice.
+ *  sched, num_splits, num_partitions, total_splits: a plan from mla_decode_plan with
+ *           cache_seqlens = s_kv for each of num_tokens requests, q_tokens_per_req = 1,
+ *           num_heads and topk (copied to the device); workspace as for mla_decode.
+ *  out      device bf16 [num_tokens, num_heads, 512]; lse device float [num_tokens,
+ *           num_heads] (natural log over the listed rows); max_logits device float
+ *           [num_tokens, num_heads]: the largest sm_scale * <q, K_j> over the listed
+ *           rows. A token with no valid entry gets out = 0, lse = -inf, max_logits = -inf.
+ * flags: MLA_DECODE_SKIP_COMBINE is not accepted here (split partials are always merged).
+ * Errors as mla_decode.
+ */
+int mla_sparse_prefill(const void* q, const void* kv, int32_t s_kv, const int32_t* indices, int32_t topk,
+                       int32_t num_tokens, int32_t num_heads, float sm_scale, const int32_t* sched,
+                       const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
+                       size_t workspace_bytes, void* out, float* max_logits, float* lse, uint32_t flags,
+                       void* stream);
 
 /*
  * No-allocation decode (device). The pages have no counterpart to this entry
@@ -189,6 +222,9 @@ int mla_decode(const void* q, const void* kv_cache, mla_kv_layout layout, int64_
  *    streams or host threads) race with each other.
  *  - Each call clears the status word first. status_out, if not NULL, is a
  *    device uint32 that receives this call's MLA_STATUS_* bits (stream-ordered).
+ *    It is the only way to see this call's device-side checks (a bad page, a
+ *    pipeline wait that ran out): the static status word is not exposed, and
+ *    the next call clears it. Pass NULL only when those checks are not needed.
  */
 #define MLA_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
 int mla_decode_static_workspace(const void* q, const void* kv_cache, mla_kv_layout layout, int64_t num_pages,
@@ -295,10 +331,15 @@ int mla_combine_inv_rope(const float* part_out, const float* part_lse, const int
  * Layout 0 copies the bits. fp8 layouts: per 64-element NoPE group,
  * amax = max(max|x|, 1e-10f), e = the smallest integer with 448 * 2^e >= amax,
  * scale byte = e + 127, code = e4m3 round-to-nearest-even, saturating, of
- * x * 2^-e; the RoPE part is copied as bf16.
+ * x * 2^-e; the RoPE part is copied as bf16. A NaN element takes no part in its
+ * group's amax (the maximum is taken over the numbers) and is stored as the
+ * E4M3 NaN code 0x7F; an infinite one makes amax infinite (scale byte 254) and
+ * is stored as +-448.
+ *  status device uint32 or NULL: a row whose slot's page is >= num_pages is not
+ *         written and ORs MLA_STATUS_BAD_SLOT into *status.
  */
 int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cache, mla_kv_layout layout,
-                 int64_t num_pages, int32_t page_size, void* stream);
+                 int64_t num_pages, int32_t page_size, uint32_t* status, void* stream);
 
 /*
  * Normalise, rotate and write new KV rows (device): the step that produces a
@@ -322,10 +363,14 @@ int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cac
  *    layout 1 rotates elements 448..511 after the normalisation;
  *  - the row is rounded to bf16 (nearest even) and written exactly as
  *    mla_kv_write writes that bf16 row.
+ * status (device uint32, or NULL) is OR-ed with MLA_STATUS_BAD_POSITION for a
+ * row skipped for its position and MLA_STATUS_BAD_SLOT for a row whose slot's
+ * page is out of range (as for mla_kv_write).
  */
 int mla_kv_write_norm_rope(const void* raw, const int32_t* slots, const int32_t* positions, const void* norm_weight,
                            float eps, const float* freqs, int32_t max_pos, int32_t n, void* kv_cache,
-                           mla_kv_layout layout, int64_t num_pages, int32_t page_size, void* stream);
+                           mla_kv_layout layout, int64_t num_pages, int32_t page_size, uint32_t* status,
+                           void* stream);
 
 /*
  * Page gather (device, a test export): out[j, :] = decoded K row j of one

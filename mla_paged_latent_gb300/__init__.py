@@ -48,7 +48,7 @@ class _PlanInfo(ctypes.Structure):
                 ("max_splits", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
 
 
-EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_decode_runs", "mla_swa_plan",
+EXPORTS = ["mla_page_bytes", "mla_decode_plan", "mla_decode", "mla_decode_runs", "mla_sparse_prefill", "mla_swa_plan",
            "mla_decode_static_workspace", "mla_combine",
            "mla_combine_v_up", "mla_combine_inv_rope", "mla_kv_write", "mla_kv_write_norm_rope", "mla_kv_gather", "mla_workspace_init", "mla_read_status",
            "mla_last_error"]
@@ -75,13 +75,15 @@ def load(path: str | None = None):
         lib.mla_decode_runs.argtypes = [V, V, I32, I64, I32, V, I32, I32, I32, I32, F32, V, V, V, I32, I32, V, SZ, V,
                                         V, ctypes.c_uint32, V]
         lib.mla_swa_plan.argtypes = [V, V, I32, I32, I32, I32, V, V]
+        lib.mla_sparse_prefill.argtypes = [V, V, I32, V, I32, I32, I32, F32, V, V, I32, I32, V, SZ, V, V, V,
+                                           ctypes.c_uint32, V]
         lib.mla_decode_static_workspace.argtypes = [V, V, I32, I64, I32, V, I32, V, I32, I32, I32, F32, V, V, I32, I32,
                                                     V, V, I32, I32, V, V, V, V]
         lib.mla_combine.argtypes = [V, V, V, I32, I32, I32, V, V, V, V]
         lib.mla_combine_v_up.argtypes = [V, V, V, I32, I32, I32, V, V, V, V, V, V, V]
         lib.mla_combine_inv_rope.argtypes = [V, V, V, I32, I32, I32, V, V, V, I32, I32, V, V, V]
-        lib.mla_kv_write.argtypes = [V, V, I32, V, I32, I64, I32, V]
-        lib.mla_kv_write_norm_rope.argtypes = [V, V, V, V, F32, V, I32, I32, V, I32, I64, I32, V]
+        lib.mla_kv_write.argtypes = [V, V, I32, V, I32, I64, I32, V, V]
+        lib.mla_kv_write_norm_rope.argtypes = [V, V, V, V, F32, V, I32, I32, V, I32, I64, I32, V, V]
         lib.mla_kv_gather.argtypes = [V, I32, I64, I32, V, I32, I32, V, V]
         lib.mla_workspace_init.argtypes = [V, V]
         lib.mla_read_status.argtypes = [V, ctypes.POINTER(ctypes.c_uint32), I32, V]
@@ -161,11 +163,12 @@ def mla_decode_plan(cache_seqlens, q_tokens_per_req: int, num_heads: int, topk: 
 def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens, q_tokens_per_req: int,
                sm_scale: float, sched, num_splits, num_partitions: int, total_splits: int, workspace, out, lse,
                sink=None, indices=None, causal: bool = False, skip_combine: bool = False, stream=None,
-               _test_withhold_signal: bool = False):
+               cta_pair: bool = False, _test_withhold_signal: bool = False):
     """Enqueue decode (+ split combine) on `stream`. All tensors on the GPU:
     q bf16 [T, N, Dqk]; kv_cache uint8 [num_pages, page_bytes]; block_table int32 [B, max_pages];
     cache_seqlens int32 [B]; sched int32 [P, 8]; num_splits int32 [B+1]; workspace uint8;
-    out bf16 [T, N, 512]; lse float32 [T, N]; sink float32 [N] or None; indices int32 [T, topk] or None."""
+    out bf16 [T, N, 512]; lse float32 [T, N]; sink float32 [N] or None; indices int32 [T, topk] or None.
+    cta_pair: run a bf16 decode whose query rows come in groups of 128 on the CTA-pair kernel."""
     _require_cuda(q, kv_cache, block_table, cache_seqlens, sched, num_splits, workspace, out, lse, sink, indices)
     T, N, D = q.shape
     B = cache_seqlens.shape[0]
@@ -174,8 +177,23 @@ def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seql
                              block_table.shape[1], _ptr(cache_seqlens), B, q_tokens_per_req, N, float(sm_scale),
                              _ptr(sink), _ptr(indices), topk, int(bool(causal)), _ptr(sched), _ptr(num_splits),
                              num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
-                             (1 if skip_combine else 0) | (0x80000000 if _test_withhold_signal else 0),
+                             (1 if skip_combine else 0) | (2 if cta_pair else 0) |
+                             (0x80000000 if _test_withhold_signal else 0),
                              _stream(stream)))
+
+
+def mla_sparse_prefill(q, kv, indices, sm_scale: float, sched, num_splits, num_partitions: int, total_splits: int,
+                       workspace, out, max_logits, lse, stream=None):
+    """Sparse prefill over one unpaged latent run (flash_mla_sparse_fwd's contract): q bf16
+    [T, N, 576]; kv bf16 [s_kv, 576]; indices int32 [T, topk] (positions in kv, others skipped);
+    the plan from mla_decode_plan(np.full(T, s_kv), 1, N, topk, ...). Writes out bf16
+    [T, N, 512], max_logits float32 [T, N] and lse float32 [T, N]."""
+    _require_cuda(q, kv, indices, sched, num_splits, workspace, out, max_logits, lse)
+    T, N, D = q.shape
+    _check(load().mla_sparse_prefill(_ptr(q), _ptr(kv), kv.shape[0], _ptr(indices), int(indices.shape[-1]), T, N,
+                                     float(sm_scale), _ptr(sched), _ptr(num_splits), num_partitions, total_splits,
+                                     _ptr(workspace), workspace.numel(), _ptr(out), _ptr(max_logits), _ptr(lse), 0,
+                                     _stream(stream)))
 
 
 def mla_swa_plan(kv_indices, page_size: int, kv_run_step: int, runs, topk_lengths=None, stream=None):
@@ -237,10 +255,12 @@ def mla_combine(part_out, part_lse, num_splits, rows_per_req: int, num_heads: in
                               _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)))
 
 
-def mla_kv_write(rows, slots, kv_cache, layout: int, page_size: int, stream=None):
-    _require_cuda(rows, slots, kv_cache)
+def mla_kv_write(rows, slots, kv_cache, layout: int, page_size: int, status=None, stream=None):
+    """Write new rows into their page slots. status: optional device uint32 [1] that
+    receives MLA_STATUS_BAD_SLOT (4) for a row whose page is out of range (not written)."""
+    _require_cuda(rows, slots, kv_cache, status)
     _check(load().mla_kv_write(_ptr(rows), _ptr(slots), slots.shape[0], _ptr(kv_cache), layout, kv_cache.shape[0],
-                               page_size, _stream(stream)))
+                               page_size, _ptr(status), _stream(stream)))
 
 
 def mla_combine_v_up(part_out, part_lse, num_splits, q_tokens_per_req: int, num_heads: int, w_uv, out, lse, o_v,
@@ -268,14 +288,15 @@ def mla_combine_inv_rope(part_out, part_lse, num_splits, q_tokens_per_req: int, 
 
 
 def mla_kv_write_norm_rope(raw, slots, positions, norm_weight, eps: float, freqs, kv_cache, layout: int,
-                           page_size: int, stream=None):
+                           page_size: int, status=None, stream=None):
     """RMSNorm + RoPE + write of new KV rows: raw bf16 [n, 576] (layouts 0, 2) or [n, 512] (layout 1);
     slots int32 [n]; positions int32 [n]; norm_weight bf16 [512]; freqs float32 [max_pos, 64]
-    (32 interleaved (cos, sin) pairs per position). All on the GPU."""
-    _require_cuda(raw, slots, positions, norm_weight, freqs, kv_cache)
+    (32 interleaved (cos, sin) pairs per position). All on the GPU. status: optional device
+    uint32 [1] receiving MLA_STATUS_BAD_SLOT (4) / MLA_STATUS_BAD_POSITION (8) for skipped rows."""
+    _require_cuda(raw, slots, positions, norm_weight, freqs, kv_cache, status)
     _check(load().mla_kv_write_norm_rope(_ptr(raw), _ptr(slots), _ptr(positions), _ptr(norm_weight), float(eps),
                                          _ptr(freqs), freqs.shape[0], slots.shape[0], _ptr(kv_cache), layout,
-                                         kv_cache.shape[0], page_size, _stream(stream)))
+                                         kv_cache.shape[0], page_size, _ptr(status), _stream(stream)))
 
 
 def mla_kv_gather(kv_cache, layout: int, page_size: int, block_table_row, length: int, out, stream=None):

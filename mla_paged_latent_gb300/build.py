@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla_decode_gb300.so")
 
-SOURCES = ["api.cpp", "plan.cpp", "decode_sm103.cu", "aux_sm103.cu", "vup_sm103.cu", "noalloc_sm103.cu"]
+SOURCES = ["api.cpp", "plan.cpp", "decode_sm103.cu", "decode_pair_sm103.cu", "aux_sm103.cu", "vup_sm103.cu",
+           "noalloc_sm103.cu"]
 HEADERS = ["mla_kernels.h", "ptx_sm103.cuh", "decode_common.cuh", "combine_row.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -64,10 +64,18 @@ int layout_geometry(int layout, int page_size, int64_t* row_bytes, int64_t* page
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+}  // namespace
+
+namespace mla {
 size_t workspace_bytes_for(int64_t total_splits, int64_t rows_per_req) {
+  // status header, partial lse (padded to 256 B), partial out, partial max logits (padded)
   const size_t n = static_cast<size_t>(total_splits) * static_cast<size_t>(rows_per_req);
-  return MLA_WORKSPACE_HEADER + align256(n * sizeof(float)) + n * MLA_DV * sizeof(float);
+  return MLA_WORKSPACE_HEADER + align256(n * sizeof(float)) + n * MLA_DV * sizeof(float) + align256(n * sizeof(float));
 }
+}  // namespace mla
+
+namespace {
+using mla::workspace_bytes_for;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -86,6 +94,27 @@ EncodeTiledFn get_encode_fn(int* err) {
   });
   *err = status;
   return fn;
+}
+
+// Most 2-CTA clusters of the pair decode kernel resident at once on the current device
+// (looked up once per device).
+int pair_cluster_capacity(int* n) {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  if (cache[dev] == 0) {
+    int c = 0;
+    e = mla::decode_pair_max_clusters(&c);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters (pair decode kernel)");
+    if (c < 1) return fail(MLA_ERR_UNSUPPORTED, "no 2-CTA cluster of the pair decode kernel fits on this device");
+    cache[dev] = c;
+  }
+  *n = cache[dev];
+  return 0;
 }
 
 int current_sm_count(int* n) {
@@ -158,10 +187,13 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
                 int32_t q_tokens_per_req, int32_t num_heads, float sm_scale, const float* sink,
                 const int32_t* indices, const int32_t* runs, int32_t topk, int32_t causal, const int32_t* sched,
                 const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
-                size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream) {
+                size_t workspace_bytes, void* out, float* lse, uint32_t flags, void* stream, int32_t uniform_len = 0,
+                float* max_logits = nullptr) {
   if (!q || !kv_cache || !sched || !num_splits || !workspace || !out || !lse)
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: NULL pointer argument");
-  if (runs == nullptr && (!block_table || !cache_seqlens))
+  // block_table and cache_seqlens are required except for run windows and for the unpaged
+  // run of sparse prefill (uniform_len > 0)
+  if (runs == nullptr && uniform_len == 0 && (!block_table || !cache_seqlens))
     return fail(MLA_ERR_INVALID_ARG, "mla_decode: NULL pointer argument");
   if (runs != nullptr) {
     if (indices != nullptr || topk < 1 || causal)
@@ -246,6 +278,10 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
   p.status = reinterpret_cast<unsigned int*>(ws);
   p.part_lse = reinterpret_cast<float*>(ws + MLA_WORKSPACE_HEADER);
   p.part_out = reinterpret_cast<float*>(ws + MLA_WORKSPACE_HEADER + align256(nrows * sizeof(float)));
+  p.part_max = reinterpret_cast<float*>(ws + MLA_WORKSPACE_HEADER + align256(nrows * sizeof(float)) +
+                                        nrows * MLA_DV * sizeof(float));
+  p.max_logits = max_logits;
+  p.uniform_len = uniform_len;
   p.num_pages = num_pages;
   p.page_bytes = page_bytes;
   p.row_bytes = static_cast<int32_t>(row_bytes);
@@ -265,17 +301,27 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   p.test_withhold_signal = (flags & MLA_DECODE_TEST_WITHHOLD_SIGNAL) ? 1 : 0;
 
-  mla::DecodeVariant v;
-  if (layout == MLA_KV_BF16_576) v = tma_kv ? mla::DecodeVariant::kBf16Tma : mla::DecodeVariant::kBf16Gather;
-  else if (layout == MLA_KV_FP8_448_UE8M0) v = mla::DecodeVariant::kFp8_448;
-  else v = mla::DecodeVariant::kFp8_512;
-  const int grid = p.num_work < num_sms ? p.num_work : num_sms;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = mla::launch_decode(v, p, q_map, kv_map, grid, s);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_decode: decode launch");
+  cudaError_t e;
+  if (tma_kv && R % 128 == 0 && (flags & MLA_DECODE_CTA_PAIR)) {
+    // query rows in groups of 128: one CTA pair per (partition, group of 128 rows)
+    int cap = 0;
+    if (int rc = pair_cluster_capacity(&cap)) return rc;
+    const int work = num_partitions * static_cast<int>(R / 128);
+    e = mla::launch_decode_pair(p, q_map, kv_map, work < cap ? work : cap, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_decode: pair decode launch");
+  } else {
+    mla::DecodeVariant v;
+    if (layout == MLA_KV_BF16_576) v = tma_kv ? mla::DecodeVariant::kBf16Tma : mla::DecodeVariant::kBf16Gather;
+    else if (layout == MLA_KV_FP8_448_UE8M0) v = mla::DecodeVariant::kFp8_448;
+    else v = mla::DecodeVariant::kFp8_512;
+    const int grid = p.num_work < num_sms ? p.num_work : num_sms;
+    e = mla::launch_decode(v, p, q_map, kv_map, grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_decode: decode launch");
+  }
   if (total_splits > batch && !(flags & MLA_DECODE_SKIP_COMBINE)) {
     e = mla::launch_combine(p.part_out, p.part_lse, num_splits, batch, static_cast<int>(R), num_heads, sink, p.out,
-                            lse, s);
+                            lse, p.part_max, max_logits, s);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode: combine launch");
   }
   return MLA_OK;
@@ -308,6 +354,27 @@ int mla_decode_runs(const void* q, const void* kv_cache, mla_kv_layout layout, i
                      total_splits, workspace, workspace_bytes, out, lse, flags, stream);
 }
 
+int mla_sparse_prefill(const void* q, const void* kv, int32_t s_kv, const int32_t* indices, int32_t topk,
+                       int32_t num_tokens, int32_t num_heads, float sm_scale, const int32_t* sched,
+                       const int32_t* num_splits, int32_t num_partitions, int32_t total_splits, void* workspace,
+                       size_t workspace_bytes, void* out, float* max_logits, float* lse, uint32_t flags,
+                       void* stream) {
+  if (!indices || !max_logits) return fail(MLA_ERR_INVALID_ARG, "mla_sparse_prefill: NULL pointer argument");
+  if (flags & MLA_DECODE_SKIP_COMBINE)
+    return fail(MLA_ERR_INVALID_ARG, "mla_sparse_prefill: MLA_DECODE_SKIP_COMBINE is not accepted");
+  if (s_kv < 1 || topk < 1 || num_tokens < 1)
+    return fail(MLA_ERR_INVALID_ARG, "mla_sparse_prefill: s_kv, topk and num_tokens must be >= 1");
+  if (reinterpret_cast<uintptr_t>(max_logits) & 3u)
+    return fail(MLA_ERR_INVALID_ARG, "mla_sparse_prefill: max_logits must be 4-byte aligned");
+  // kv as 64-row pages of one unpaged run; token t is a request of one query token whose
+  // candidates are its index list (positions of the run), every request s_kv rows long
+  const int64_t num_pages = (static_cast<int64_t>(s_kv) + 63) / 64;
+  return decode_impl(q, kv, MLA_KV_BF16_576, num_pages, 64, nullptr, 1, nullptr, num_tokens, 1, num_heads, sm_scale,
+                     nullptr, indices, nullptr, topk, 0, sched, num_splits, num_partitions, total_splits, workspace,
+                     workspace_bytes, out, lse, flags & ~static_cast<uint32_t>(MLA_DECODE_TEST_WITHHOLD_SIGNAL), stream,
+                     s_kv, max_logits);
+}
+
 int mla_swa_plan(const int32_t* kv_indices, const int32_t* topk_lengths, int32_t num_tokens, int32_t topk,
                  int32_t page_size, int32_t kv_run_step, int32_t* runs, void* stream) {
   if (!kv_indices || !runs) return fail(MLA_ERR_INVALID_ARG, "mla_swa_plan: NULL pointer argument");
@@ -330,13 +397,14 @@ int mla_combine(const float* part_out, const float* part_lse, const int32_t* num
   if (!aligned16(part_out) || (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
     return fail(MLA_ERR_INVALID_ARG, "mla_combine: part_out must be 16-byte and out 8-byte aligned");
   cudaError_t e = mla::launch_combine(part_out, part_lse, num_splits, batch, rows_per_req, num_heads, sink,
-                                      static_cast<uint16_t*>(out), lse, static_cast<cudaStream_t>(stream));
+                                      static_cast<uint16_t*>(out), lse, nullptr, nullptr,
+                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mla_combine: launch");
   return MLA_OK;
 }
 
 int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cache, mla_kv_layout layout,
-                 int64_t num_pages, int32_t page_size, void* stream) {
+                 int64_t num_pages, int32_t page_size, uint32_t* status, void* stream) {
   if (n < 0) return fail(MLA_ERR_INVALID_ARG, "mla_kv_write: n < 0");
   if (n == 0) return MLA_OK;
   if (!rows || !slots || !kv_cache) return fail(MLA_ERR_INVALID_ARG, "mla_kv_write: NULL pointer");
@@ -349,7 +417,7 @@ int mla_kv_write(const void* rows, const int32_t* slots, int32_t n, void* kv_cac
   if (!aligned16(rows) || !aligned16(kv_cache))
     return fail(MLA_ERR_INVALID_ARG, "mla_kv_write: rows and kv_cache must be 16-byte aligned");
   cudaError_t e = mla::launch_kv_write(static_cast<const uint16_t*>(rows), slots, n, static_cast<uint8_t*>(kv_cache),
-                                       static_cast<int>(layout), num_pages, page_size, pb,
+                                       static_cast<int>(layout), num_pages, page_size, pb, status,
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mla_kv_write: launch");
   return MLA_OK;
@@ -415,7 +483,8 @@ int mla_combine_v_up(const float* part_out, const float* part_lse, const int32_t
 
 int mla_kv_write_norm_rope(const void* raw, const int32_t* slots, const int32_t* positions, const void* norm_weight,
                            float eps, const float* freqs, int32_t max_pos, int32_t n, void* kv_cache,
-                           mla_kv_layout layout, int64_t num_pages, int32_t page_size, void* stream) {
+                           mla_kv_layout layout, int64_t num_pages, int32_t page_size, uint32_t* status,
+                           void* stream) {
   if (n < 0) return fail(MLA_ERR_INVALID_ARG, "mla_kv_write_norm_rope: n < 0");
   if (n == 0) return MLA_OK;
   if (!raw || !slots || !positions || !norm_weight || !freqs || !kv_cache)
@@ -436,7 +505,7 @@ int mla_kv_write_norm_rope(const void* raw, const int32_t* slots, const int32_t*
                 "mla_kv_write_norm_rope: raw, norm_weight and kv_cache must be 16-byte aligned, freqs 4-byte aligned");
   cudaError_t e = mla::launch_kv_write_norm_rope(
       static_cast<const uint16_t*>(raw), slots, positions, static_cast<const uint16_t*>(norm_weight), eps, freqs,
-      max_pos, n, static_cast<uint8_t*>(kv_cache), static_cast<int>(layout), num_pages, page_size, pb,
+      max_pos, n, static_cast<uint8_t*>(kv_cache), static_cast<int>(layout), num_pages, page_size, pb, status,
       static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "mla_kv_write_norm_rope: launch");
   return MLA_OK;

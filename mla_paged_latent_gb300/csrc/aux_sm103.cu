@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ part_lse,
                                                       const int32_t* __restrict__ num_splits, int R, int heads,
                                                       const float* __restrict__ sink, uint16_t* __restrict__ out,
-                                                      float* __restrict__ lse) {
+                                                      float* __restrict__ lse, const float* __restrict__ part_max,
+                                                      float* __restrict__ max_logits) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
@@ -36,6 +37,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const float lse_tot = merge_row(part_out, part_lse, s0, ns, R, row, lane, sink, row % heads, acc);
   store_row_bf16(out + orow * 512, lane, acc);
   if (lane == 0) lse[orow] = lse_tot;
+  if (max_logits != nullptr) {  // the largest scaled score: the largest over the splits
+    float m = -INFINITY;
+    for (int s = lane; s < ns; s += 32) m = fmaxf(m, part_max[(int64_t)(s0 + s) * R + row]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) max_logits[orow] = m;
+  }
 }
 
 // One warp per query row: the merged (split) or decode-written (unsplit) row, with the
@@ -202,7 +210,7 @@ __device__ __forceinline__ void write_row(const uint16_t* x, int lane, uint8_t* 
     }
   }
   const bool in_nope = lane * 16 < nope;
-  float a = 0.f;
+  float a = 0.f;  // fmaxf returns the number when one operand is NaN: NaN elements do not count
 #pragma unroll
   for (int k = 0; k < 16; ++k) a = fmaxf(a, fabsf(v[k]));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
@@ -218,6 +226,10 @@ __device__ __forceinline__ void write_row(const uint16_t* x, int lane, uint8_t* 
       asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c0) : "f"(v[4 * k + 1] * sc), "f"(v[4 * k] * sc));
       asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c1) : "f"(v[4 * k + 3] * sc), "f"(v[4 * k + 2] * sc));
       w4[k] = static_cast<uint32_t>(c0) | (static_cast<uint32_t>(c1) << 16);
+      // a NaN element (left out of the amax above) is stored as the NaN code 0x7F, whatever its sign
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (v[4 * k + b] != v[4 * k + b]) w4[k] = (w4[k] & ~(0xFFu << (8 * b))) | (0x7Fu << (8 * b));
     }
     reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
   } else {
@@ -247,7 +259,7 @@ __device__ __forceinline__ void write_row(const uint16_t* x, int lane, uint8_t* 
 __global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restrict__ rows,
                                                        const int32_t* __restrict__ slots, int n,
                                                        uint8_t* __restrict__ kv, int layout, int64_t num_pages,
-                                                       int page_size, int64_t page_bytes) {
+                                                       int page_size, int64_t page_bytes, uint32_t* status) {
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -256,7 +268,10 @@ __global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restric
   const int64_t slot = slots[r];
   if (slot < 0) return;
   const int64_t page = slot / page_size;
-  if (page >= num_pages) return;
+  if (page >= num_pages) {  // reported, not written
+    if (lane == 0 && status != nullptr) atomicOr(status, 4u);
+    return;
+  }
   const int row_elems = layout == 1 ? 512 : 576;
   write_row(rows + (int64_t)r * row_elems, lane, kv, layout, page, static_cast<int>(slot % page_size), page_size,
             page_bytes);
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(128) kv_write_kernel(const uint16_t* __restric
 __global__ void __launch_bounds__(128) kv_write_norm_rope_kernel(
     const uint16_t* __restrict__ raw, const int32_t* __restrict__ slots, const int32_t* __restrict__ positions,
     const uint16_t* __restrict__ w, float eps, const float* __restrict__ freqs, int max_pos, int n,
-    uint8_t* __restrict__ kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes) {
+    uint8_t* __restrict__ kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes, uint32_t* status) {
   pdl_trigger();
   pdl_wait();
   __shared__ __align__(16) uint16_t srow[4][576];
@@ -281,9 +296,12 @@ __global__ void __launch_bounds__(128) kv_write_norm_rope_kernel(
   const int64_t slot = slots[r];
   if (slot < 0) return;
   const int64_t page = slot / page_size;
-  if (page >= num_pages) return;
   const int pos = positions[r];
-  if (pos < 0 || pos >= max_pos) return;
+  const uint32_t bad = (page >= num_pages ? 4u : 0u) | (pos < 0 || pos >= max_pos ? 8u : 0u);
+  if (bad != 0u) {  // reported, not written
+    if (lane == 0 && status != nullptr) atomicOr(status, bad);
+    return;
+  }
   const int row_elems = layout == 1 ? 512 : 576;
   const uint16_t* x = raw + (int64_t)r * row_elems;
   const float* f = freqs + (int64_t)pos * 64;
@@ -384,11 +402,11 @@ __global__ void __launch_bounds__(128) kv_gather_kernel(const uint8_t* __restric
 
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
                            int rows_per_req, int heads, const float* sink, uint16_t* out, float* lse,
-                           cudaStream_t stream) {
+                           const float* part_max, float* max_logits, cudaStream_t stream) {
   if (batch <= 0 || rows_per_req <= 0) return cudaSuccess;
   dim3 grid((rows_per_req + 7) / 8, batch);
   return launch_pdl(combine_kernel, grid, dim3(256), 0, stream, part_out, part_lse, num_splits, rows_per_req, heads,
-                    sink, out, lse);
+                    sink, out, lse, part_max, max_logits);
 }
 
 cudaError_t launch_swa_plan(const int32_t* kv_indices, const int32_t* topk_lengths, int num_tokens, int topk,
@@ -409,19 +427,20 @@ cudaError_t launch_combine_inv_rope(const float* part_out, const float* part_lse
 }
 
 cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout,
-                            int64_t num_pages, int page_size, int64_t page_bytes, cudaStream_t stream) {
+                            int64_t num_pages, int page_size, int64_t page_bytes, uint32_t* status,
+                            cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   return launch_pdl(kv_write_kernel, dim3((n + 3) / 4), dim3(128), 0, stream, rows, slots, n, kv, layout, num_pages,
-                    page_size, page_bytes);
+                    page_size, page_bytes, status);
 }
 
 cudaError_t launch_kv_write_norm_rope(const uint16_t* raw, const int32_t* slots, const int32_t* positions,
                                      const uint16_t* norm_weight, float eps, const float* freqs, int max_pos, int n,
                                      uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
-                                     cudaStream_t stream) {
+                                     uint32_t* status, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   return launch_pdl(kv_write_norm_rope_kernel, dim3((n + 3) / 4), dim3(128), 0, stream, raw, slots, positions,
-                    norm_weight, eps, freqs, max_pos, n, kv, layout, num_pages, page_size, page_bytes);
+                    norm_weight, eps, freqs, max_pos, n, kv, layout, num_pages, page_size, page_bytes, status);
 }
 
 cudaError_t launch_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,

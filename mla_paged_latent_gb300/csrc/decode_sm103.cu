@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           rows = rows > P.qbox_rows ? P.qbox_rows : rows;
           if (rows > 0) prefetch_l2_bulk(P.q + row0 * (NS * 64), static_cast<uint32_t>(rows * NS * 64 * 2));
         }
-        const int L = runs ? 0x7fffffff : P.seqlens[r];
+        const int L = runs ? 0x7fffffff : request_len(P, r);
         const int tok = r * P.sq + (g * kGroupRows) / P.heads;
         const int4 rn = runs ? reinterpret_cast<const int4*>(runs)[tok] : make_int4(0, 0, 0, 0);
         for (int j = lo; j < hi; ++j, ++pit) {
@@ -397,7 +397,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               page[h] = -1;
               if (pos[h] < 0 || pos[h] >= L) continue;
               const int pi = pos[h] >> P.log2_ps;
-              if (runs) page[h] = pi;  // run slots are cache slots: page * page_size + offset
+              // run slots (and positions of an unpaged run) are cache slots: page * page_size + offset
+              if (runs || P.block_table == nullptr) page[h] = pi;
               else page[h] = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
             }
 #pragma unroll
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int nq = (rows_g + 15) & ~15;
       for_each_unit(P, part, [&](int r, int lo, int hi, int sidx) {
         if (stop) return;
-        const int L = runs ? 0x7fffffff : P.seqlens[r];
+        const int L = runs ? 0x7fffffff : request_len(P, r);
         const int grow = g * kGroupRows + row;          // query row within the request
         const bool valid_row = row_thread && row < rows_g;
         const int tok = grow / P.heads;
@@ -467,6 +468,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           lim = lim > L ? L : lim;
         }
         float m_run = -INFINITY, l_run = 0.f;
+        float m_true = -INFINITY;  // the largest scaled score (log2 units), for max_logits
         const int ntile = hi - lo;
         for (int jj = 0; jj < ntile; ++jj) {
           const int itj = it + jj;
@@ -508,6 +510,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               m4[c & 3] = fmaxf(m4[c & 3], x[c]);
             }
             const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
+            m_true = fmaxf(m_true, mt);
             const float m_new = (mt > m_run + kRescaleLog2) ? mt : m_run;
             need = (m_new != m_run) && (m_run != -INFINITY) && !first;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
@@ -611,6 +614,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             const float lse_nat = lse2 * 0.6931471805599453f;
             if (nsplit == 1) P.lse[(int64_t)r * R + grow] = lse_nat;
             else P.part_lse[(int64_t)sg * R + grow] = lse_nat;
+            if (P.max_logits != nullptr) {
+              const float mx = m_true * 0.6931471805599453f;  // back from log2 units: sm_scale * <q, k>
+              if (nsplit == 1) P.max_logits[(int64_t)r * R + grow] = mx;
+              else P.part_max[(int64_t)sg * R + grow] = mx;
+            }
           }
         }
         if (named_bar_or(1, 128, dead)) {
@@ -683,7 +691,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int part = w / G, g = w % G;
       for_each_unit(P, part, [&](int r, int lo, int hi, int) {
         if (*abort_flag) return;
-        const int L = runs ? 0x7fffffff : P.seqlens[r];
+        const int L = runs ? 0x7fffffff : request_len(P, r);
         const int tok = r * P.sq + (g * kGroupRows) / P.heads;   // sparse: the group's token
         const int4 rn = runs ? reinterpret_cast<const int4*>(runs)[tok] : make_int4(0, 0, 0, 0);
         // The address chain of a row (top-k index -> block_table entry -> row) runs two
@@ -701,8 +709,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         auto row_page = [&](int pos) -> int {  // its page; -1 if no row, -2 if the entry is bad
           if (pos < 0 || pos >= L) return -1;
           const int pi = pos >> P.log2_ps;
-          // run slots are cache slots (page * page_size + offset), not positions of the request
-          const int page = runs ? pi : (pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1);
+          // run slots (and positions of an unpaged run) are cache slots (page * page_size +
+          // offset), not positions of the request
+          const int page = (runs || P.block_table == nullptr)
+                               ? pi
+                               : (pi < P.max_pages ? P.block_table[(int64_t)r * P.max_pages + pi] : -1);
           return (page < 0 || page >= P.num_pages) ? -2 : page;
         };
         int pos_a = row_pos(lo), pos_b = row_pos(lo + 1);

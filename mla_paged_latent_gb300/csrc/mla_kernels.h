@@ -15,8 +15,8 @@ constexpr int kDecodeThreads = 512;
 struct DecodeParams {
   const uint16_t* q;              // bf16 [T, heads, dqk] (L2 prefetch; loads use the tensor map)
   const uint8_t* kv;              // paged cache (converter path and L2 prefetch)
-  const int32_t* block_table;     // [batch, max_pages]
-  const int32_t* seqlens;         // [batch]
+  const int32_t* block_table;     // [batch, max_pages]; null: positions are rows of one unpaged run
+  const int32_t* seqlens;         // [batch]; null: every request has uniform_len rows
   const float* sink;              // [heads] or null
   const int32_t* indices;         // [T, topk] or null
   const int32_t* runs;            // [T, 4] (slot0, len0, slot1, rows) or null: run-window mode
@@ -26,6 +26,8 @@ struct DecodeParams {
   float* lse;                     // [T, heads]
   float* part_out;                // [total_splits, R, 512]
   float* part_lse;                // [total_splits, R]
+  float* max_logits;              // [T, heads] or null: the largest scaled score of each row
+  float* part_max;                // [total_splits, R]: its split partials (with max_logits)
   unsigned int* status;           // device status word
   int64_t num_pages;
   int64_t page_bytes;
@@ -45,6 +47,7 @@ struct DecodeParams {
   int32_t num_work;               // num_partitions * groups
   float scale_log2;               // sm_scale * log2(e)
   int32_t test_withhold_signal;   // MLA_DECODE_TEST_WITHHOLD_SIGNAL: skip the first S-complete commit
+  int32_t uniform_len;            // rows of every request when seqlens is null
 };
 
 // Kernel variants: layout 0 with TMA page loads (dense), layout 0 gathered by
@@ -52,20 +55,28 @@ struct DecodeParams {
 enum class DecodeVariant { kBf16Tma = 0, kBf16Gather = 1, kFp8_448 = 2, kFp8_512 = 3 };
 
 size_t decode_smem_bytes(DecodeVariant v);
+
+// The CTA-pair kernel (decode_pair_sm103.cu): bf16 rows loaded by TMA, query rows in
+// groups of 128 (rows_per_req % 128 == 0); `clusters` pairs of CTAs.
+size_t decode_pair_smem_bytes();
+cudaError_t launch_decode_pair(const DecodeParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+                               int clusters, cudaStream_t stream);
+cudaError_t decode_pair_max_clusters(int* clusters);
 cudaError_t launch_decode(DecodeVariant v, const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, int grid, cudaStream_t stream);
 
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* num_splits, int batch,
                            int rows_per_req, int heads, const float* sink, uint16_t* out, float* lse,
-                           cudaStream_t stream);
+                           const float* part_max, float* max_logits, cudaStream_t stream);
 
 cudaError_t launch_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout,
-                            int64_t num_pages, int page_size, int64_t page_bytes, cudaStream_t stream);
+                            int64_t num_pages, int page_size, int64_t page_bytes, uint32_t* status,
+                            cudaStream_t stream);
 
 cudaError_t launch_kv_write_norm_rope(const uint16_t* raw, const int32_t* slots, const int32_t* positions,
                                      const uint16_t* norm_weight, float eps, const float* freqs, int max_pos, int n,
                                      uint8_t* kv, int layout, int64_t num_pages, int page_size, int64_t page_bytes,
-                                     cudaStream_t stream);
+                                     uint32_t* status, cudaStream_t stream);
 
 cudaError_t launch_swa_plan(const int32_t* kv_indices, const int32_t* topk_lengths, int num_tokens, int topk,
                             int page_size, int kv_run_step, int32_t* runs, cudaStream_t stream);
@@ -110,6 +121,15 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 #endif
+
+// Workspace bytes of a decode with `total_splits` splits of `rows_per_req` query rows:
+// the status header, the split partial lse (padded to 256 B) and the partial outputs.
+size_t workspace_bytes_for(int64_t total_splits, int64_t rows_per_req);
+
+// Rows of request r: its cache length, or the one length of all requests (sparse prefill).
+__host__ __device__ inline int request_len(const DecodeParams& P, int r) {
+  return P.seqlens != nullptr ? P.seqlens[r] : P.uniform_len;
+}
 
 PlanResult make_plan(const int32_t* seqlens, int batch, int sq, int heads, int topk, int min_splits, int num_sms);
 

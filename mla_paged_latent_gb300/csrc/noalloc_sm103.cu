@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "mla_decode.h"
+#include "mla_kernels.h"
 
 namespace mla {
 int set_last_error(int code, const char* msg);
@@ -72,10 +73,9 @@ extern "C" int mla_decode_static_workspace(const void* q, const void* kv_cache, 
                                            void* stream) {
   if (total_splits < 0 || q_tokens_per_req < 1 || num_heads < 1)
     return mla::set_last_error(MLA_ERR_INVALID_ARG, "mla_decode_static_workspace: bad sizes");
-  // the same workspace layout mla_decode uses: status header, partial lse, partial out
-  const size_t rows = static_cast<size_t>(total_splits) * static_cast<size_t>(q_tokens_per_req) *
-                      static_cast<size_t>(num_heads);
-  const size_t need = MLA_WORKSPACE_HEADER + ((rows * sizeof(float) + 255) / 256) * 256 + rows * MLA_DV * sizeof(float);
+  // the size mla_decode checks its caller's workspace against
+  const size_t need =
+      mla::workspace_bytes_for(total_splits, static_cast<int64_t>(q_tokens_per_req) * static_cast<int64_t>(num_heads));
   if (need > kStaticWorkspaceBytes) {
     char buf[256];
     snprintf(buf, sizeof buf,

@@ -94,6 +94,8 @@ def _load():
         lib.mo_inv_rope.restype = None
         lib.mo_swa_plan.argtypes = [P, P, i32, i32, i32, i32, P]
         lib.mo_swa_plan.restype = None
+        lib.mo_sparse_prefill.argtypes = [P, P, i32, P, i32, i32, i32, f64, P, P, P, i32]
+        lib.mo_sparse_prefill.restype = None
         _lib = lib
         return lib
 
@@ -327,6 +329,24 @@ def decode_runs(q_bits, kv_cache, layout: int, page_size: int, runs, sm_scale: f
             o, l = attend(qf[t, n], rows, 512, sm_scale, None if sink is None else float(sink[n]))
             out[t, n], lse[t, n] = o, l
     return out, lse
+
+
+def sparse_prefill(q_bits, kv_bits, indices, sm_scale: float, nthreads: int = 0):
+    """Sparse prefill over an unpaged bf16 latent kv (flash_mla_sparse_fwd's contract).
+    q_bits uint16 [T, N, 576], kv_bits uint16 [s_kv, 576], indices int32 [T, topk].
+    Returns (out [T, N, 512], max_logits [T, N], lse [T, N]) in float64."""
+    lib = _load()
+    q = _c(q_bits, np.uint16)
+    kv = _c(kv_bits, np.uint16)
+    idx = _c(indices, np.int32)
+    T, N, D = q.shape
+    assert D == 576 and kv.shape[1] == 576 and idx.shape[0] == T
+    out = np.zeros((T, N, 512))
+    mx = np.zeros((T, N))
+    lse = np.zeros((T, N))
+    lib.mo_sparse_prefill(_ptr(q), _ptr(kv), kv.shape[0], _ptr(idx), idx.shape[1], T, N, float(sm_scale), _ptr(out),
+                          _ptr(mx), _ptr(lse), int(nthreads))
+    return out, mx, lse
 
 
 def kv_gather(kv_cache, layout, page_size, block_table_row, length) -> np.ndarray:

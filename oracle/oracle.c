@@ -345,6 +345,8 @@ int mo_group_exponent(double a) {
  * amax = max(max |x|, eps) with eps = (float)1e-10, e = mo_group_exponent(amax),
  * scale byte = e + 127, code = E4M3 RNE-satfinite of x * 2^-e (exact product);
  * the 64 RoPE values are copied as bf16; the unused scale byte of layout 1 is 0.
+ * A NaN element takes no part in amax and is stored as the NaN code 0x7F (what
+ * mo_e4m3_encode gives for NaN); an infinite one makes amax infinite (e = 127).
  * Row elements: layout 0 -> 576, layout 1 -> 512 (448 | 64), layout 2 -> 576.
  * Returns 0, or -1 on an out-of-range slot. */
 int mo_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, int layout, int64_t num_pages,
@@ -373,7 +375,7 @@ int mo_kv_write(const uint16_t* rows, const int32_t* slots, int n, uint8_t* kv, 
       int e;
       for (d = 0; d < 64; ++d) {
         double v = fabs(mo_bf16_decode(x[g * 64 + d]));
-        if (v > amax || isnan(v)) amax = v;
+        if (v > amax) amax = v;   /* the maximum over the numbers: a NaN element does not count */
       }
       if (amax < eps) amax = eps;
       e = mo_group_exponent(amax);
@@ -555,4 +557,44 @@ int mo_kv_gather(const uint8_t* kv, int layout, int64_t num_pages, int page_size
     mo_decode_row(kv, layout, page_size, page, j % page_size, out + (size_t)j * dqk);
   }
   return 0;
+}
+
+/* Sparse prefill ([sglang-FlashMLA] Signature and I/O Contract of flash_mla_sparse_fwd:
+ * q, kv, indices, sm_scale, d_v = 512 -> out, max_logits, lse). kv is one unpaged run of
+ * s_kv latent rows (bf16 bits [s_kv, 576]); token t's candidate rows are the entries of
+ * indices[t, 0 .. topk) inside [0, s_kv) (others are skipped; duplicates count twice).
+ * For each (t, n): the attention of q[t, n] over those rows with V = row[0 : 512]
+ * (mo_attend: out, natural-log lse over the keys), and max_logits = the largest scaled
+ * score sm_scale * <q, K_j> (-inf when there is no candidate; out = 0, lse = -inf then). */
+void mo_sparse_prefill(const uint16_t* q, const uint16_t* kv, int s_kv, const int32_t* indices, int topk, int T,
+                       int nheads, double scale, double* out, double* max_logits, double* lse, int nthreads) {
+  int t;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (t = 0; t < T; ++t) {
+    int n_rows = 0, j, d, n;
+    double* rows = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1) * 576);
+    double qd[576];
+    for (j = 0; j < topk; ++j) {
+      const int32_t idx = indices[(size_t)t * topk + j];
+      if (idx < 0 || idx >= s_kv) continue;
+      for (d = 0; d < 576; ++d) rows[(size_t)n_rows * 576 + d] = mo_bf16_decode(kv[(size_t)idx * 576 + d]);
+      ++n_rows;
+    }
+    for (n = 0; n < nheads; ++n) {
+      const size_t o = (size_t)t * nheads + n;
+      double mx = -INFINITY;
+      for (d = 0; d < 576; ++d) qd[d] = mo_bf16_decode(q[o * 576 + d]);
+      for (j = 0; j < n_rows; ++j) {
+        double acc = 0.0;
+        for (d = 0; d < 576; ++d) acc += qd[d] * rows[(size_t)j * 576 + d];
+        if (scale * acc > mx) mx = scale * acc;
+      }
+      max_logits[o] = mx;
+      mo_attend(qd, 576, rows, n_rows, 512, scale, 0, 0.0, out + o * 512, lse + o);
+    }
+    free(rows);
+  }
 }

@@ -8,11 +8,20 @@ import mla_paged_latent_gb300 as mla
 import oracle
 
 # Tolerances of the decode outputs: max abs error 1e-2, relative L2 5e-3, lse
-# abs error 1e-3. The elementwise bound is read as 1e-2 * max(1, |ref|): one
-# bf16 half-ulp of the output alone exceeds 1e-2 once |out| > 2.
+# abs error 1e-3. For bf16 KV rows ("flat") the max abs error 1e-2 is asserted as
+# stated wherever |ref| <= 2; above 2 one bf16 half-step of the output alone is
+# 2^-7 = 0.0078 (and 0.0156 above 4), so there the bound is 1e-2 * |ref| (attention
+# outputs that large come only from a handful of keys or a one-hot softmax). For fp8
+# rows, whose group scales reach 2^4 so that |out| often exceeds 2, the elementwise
+# bound is 1e-2 * max(1, |ref|) throughout ("scaled").
 OUT_ABS = 1e-2
 OUT_REL_L2 = 5e-3
 LSE_ABS = 1e-3
+
+
+def bound_for(layout: int) -> str:
+    """The max-abs reading that applies to outputs over KV rows of this layout."""
+    return "flat" if layout == 0 else "scaled"
 
 
 def bf16_tensor(bits: np.ndarray, device="cuda"):
@@ -85,12 +94,16 @@ def oracle_decode(w, kv=None, select=None):
                              sink=w.sink, indices=w.indices, causal=c.causal, select=select)
 
 
-def assert_close(out, lse, ref_out, ref_lse, what=""):
+def assert_close(out, lse, ref_out, ref_lse, what="", bound="flat"):
+    """bound="flat": |out - ref| <= 1e-2 where |ref| <= 2 (1e-2 * |ref| above);
+    bound="scaled": <= 1e-2 * max(1, |ref|). Returns the raw max abs error."""
+    assert bound in ("flat", "scaled")
     out = np.asarray(out, dtype=np.float64)
     ref_out = np.asarray(ref_out, dtype=np.float64)
     assert np.all(np.isfinite(out)), f"{what}: non-finite output"
     err = np.abs(out - ref_out)
-    bound = OUT_ABS * np.maximum(1.0, np.abs(ref_out))
+    a = np.abs(ref_out)
+    bound = OUT_ABS * (np.maximum(1.0, a) if bound == "scaled" else np.where(a <= 2.0, 1.0, a))
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
     assert np.all(err <= bound), f"{what}: max abs err {err.max():.3g} (at {worst}: {out[worst]} vs {ref_out[worst]})"
     nref = np.linalg.norm(ref_out)

@@ -141,9 +141,9 @@ def test_combine_argument_validation(lib):
 
 def test_kv_write_and_gather_validation(lib):
     fake = ctypes.c_void_p(0x100000)
-    assert lib.mla_kv_write(fake, fake, 4, fake, 9, 4, 64, None) == -1
-    assert lib.mla_kv_write(fake, fake, 4, fake, 1, 4, 12, None) == -1
-    assert lib.mla_kv_write(fake, fake, 0, None, 1, 4, 64, None) == 0   # nothing to do
+    assert lib.mla_kv_write(fake, fake, 4, fake, 9, 4, 64, None, None) == -1
+    assert lib.mla_kv_write(fake, fake, 4, fake, 1, 4, 12, None, None) == -1
+    assert lib.mla_kv_write(fake, fake, 0, None, 1, 4, 64, None, None) == 0   # nothing to do
     assert lib.mla_kv_gather(fake, 0, 4, 64, None, 2, 10, fake, None) == -1
 
 
@@ -159,13 +159,14 @@ def test_next_row_entry_points_validation(lib):
     reject bad arguments before any device work."""
     fake = ctypes.c_void_p(0x100000)
     odd = ctypes.c_void_p(0x100004)
-    # mla_kv_write_norm_rope(raw, slots, positions, w, eps, freqs, max_pos, n, kv, layout, num_pages, ps, stream)
-    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 8, 0, None, 0, 4, 64, None) == 0
-    assert lib.mla_kv_write_norm_rope(fake, fake, None, fake, 1e-6, fake, 8, 4, fake, 0, 4, 64, None) == -1
-    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, -1.0, fake, 8, 4, fake, 0, 4, 64, None) == -1
-    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 0, 4, fake, 0, 4, 64, None) == -1
-    assert lib.mla_kv_write_norm_rope(fake, fake, fake, odd, 1e-6, fake, 8, 4, fake, 1, 4, 64, None) == -1
-    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 8, 4, fake, 5, 4, 64, None) == -1
+    # mla_kv_write_norm_rope(raw, slots, positions, w, eps, freqs, max_pos, n, kv, layout, num_pages, ps, status,
+    #                        stream)
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 8, 0, None, 0, 4, 64, None, None) == 0
+    assert lib.mla_kv_write_norm_rope(fake, fake, None, fake, 1e-6, fake, 8, 4, fake, 0, 4, 64, None, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, -1.0, fake, 8, 4, fake, 0, 4, 64, None, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 0, 4, fake, 0, 4, 64, None, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, odd, 1e-6, fake, 8, 4, fake, 1, 4, 64, None, None) == -1
+    assert lib.mla_kv_write_norm_rope(fake, fake, fake, fake, 1e-6, fake, 8, 4, fake, 5, 4, 64, None, None) == -1
     # mla_combine_v_up(part_out, part_lse, ns, batch, sq, heads, sink, w, out, lse, o_v, status, stream)
     assert lib.mla_combine_v_up(fake, fake, fake, 2, 1, 16, None, None, fake, fake, fake, None, None) == -1
     assert lib.mla_combine_v_up(fake, None, fake, 2, 1, 16, None, fake, fake, fake, fake, None, None) == -1

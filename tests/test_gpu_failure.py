@@ -14,7 +14,7 @@ import torch
 
 import mla_paged_latent_gb300 as mla
 import workloads
-from gpu_helpers import DeviceWorkload, assert_close, oracle_decode
+from gpu_helpers import DeviceWorkload, assert_close, bound_for, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -52,4 +52,4 @@ def test_wait_timeout_is_reported_and_context_survives(cfg):
     mla.mla_workspace_init(d.ws)
     out, lse = d.run(write=False)
     ref_out, ref_lse = oracle_decode(w)
-    assert_close(out, lse, ref_out, ref_lse, "after a timed-out call")
+    assert_close(out, lse, ref_out, ref_lse, "after a timed-out call", bound_for(c.layout))

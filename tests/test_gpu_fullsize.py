@@ -10,7 +10,7 @@ import torch
 import mla_paged_latent_gb300 as mla
 import oracle
 import workloads
-from gpu_helpers import DeviceWorkload, assert_close
+from gpu_helpers import DeviceWorkload, assert_close, bound_for
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,7 @@ def test_full_size_sampled(name):
     t, n = _sample(w, rng)
     ref_out, ref_lse = oracle.mla_decode(w.q, kv_ref, c.layout, c.page_size, w.block_table, w.seqlens, c.sq,
                                          c.sm_scale, sink=w.sink, indices=w.indices, causal=c.causal, select=(t, n))
-    assert_close(out[t, n], lse[t, n], ref_out, ref_lse, f"{name} full size, sampled rows")
+    assert_close(out[t, n], lse[t, n], ref_out, ref_lse, f"{name} full size, sampled rows", bound_for(c.layout))
 
 
 def test_full_size_combine_v_up_sampled():
@@ -97,5 +97,6 @@ def test_full_size_combine_v_up_sampled():
         ref = torch.from_numpy(oracle.v_up(x_bits[k][None, None, :], w_bits[n[k]][None])[0, 0].view(np.int16).copy())
         ref = ref.view(torch.bfloat16).double().numpy()
         g = got[t[k], n[k]]
-        # the decode's own error (R12) carried through W: compare as the decode is compared
+        # the decode's own error carried through W (|o_v| stays well below 2 here): the flat
+        # 1e-2 bound of the bf16 decode outputs
         assert_close(g[None], np.zeros(1), ref[None], np.zeros(1), f"o_v row {(int(t[k]), int(n[k]))}")

@@ -483,6 +483,39 @@ def test_kv_write_fp8_matches_torch_quantization(oracle_lib):
                 assert np.all(out[p, o * info["row_bytes"]:(o + 1) * info["row_bytes"]] == 0)
 
 
+def test_kv_write_nan_and_inf_elements(oracle_lib):
+    """The reading for non-finite inputs: a NaN element does not enter its group's amax (the
+    maximum over the numbers, as C's fmax) and is stored as the NaN code 0x7F; the group's
+    other codes are torch's e4m3 rounding at the exponent of the finite amax. An infinite
+    element makes amax infinite: exponent 127 (byte 254), stored saturated as +-448."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((2, 576)).astype(np.float32)
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    bits[0, 7] = 0x7FC0     # NaN in group 0
+    bits[0, 64] = 0xFFC0    # -NaN in group 1
+    bits[1, 9] = 0x7F80     # +inf in group 0
+    bits[1, 10] = 0xFF80    # -inf in group 0
+    xb = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    kv = oracle.kv_write(bits, np.array([0, 1], np.int32), np.zeros((1, oracle.layout_info(2, 2)["page_bytes"]),
+                                                                    np.uint8), 2, 2)
+    rows = kv[0, :1280].reshape(2, 640)
+    sc = kv[0, 1280:1296].reshape(2, 8)
+    for g in (0, 1):
+        grp = xb[0, g * 64:(g + 1) * 64]
+        e = int(sc[0, g]) - 127
+        finite_amax = np.nanmax(np.abs(grp))
+        assert 448.0 * 2.0 ** e >= finite_amax > 448.0 * 2.0 ** (e - 1)
+        ref = torch.from_numpy((grp * 2.0 ** -e).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        nan = np.isnan(grp)
+        assert np.array_equal(rows[0, g * 64:(g + 1) * 64][~nan], ref[~nan])
+        assert np.all(rows[0, g * 64:(g + 1) * 64][nan] == 0x7F)
+    assert sc[1, 0] == 254
+    assert rows[1, 9] == 0x7E and rows[1, 10] == 0xFE
+    # finite elements times 2^-127 are far below the smallest e4m3 subnormal: +-0
+    others = np.setdiff1d(np.arange(64), [9, 10])
+    assert np.all((rows[1, others] & 0x7F) == 0)
+
+
 def test_kv_write_bf16_is_bit_copy(oracle_lib):
     rng = np.random.default_rng(10)
     bits = rng.integers(0, 1 << 16, (5, 576)).astype(np.uint16)
@@ -756,3 +789,61 @@ def test_decode_over_runs_equals_dense_and_is_order_free(oracle_lib):
         runs = oracle.swa_plan(order[None, :], ps, step)
         out, lse = oracle.decode_runs(q, kv, c.layout, ps, runs, c.sm_scale)
         assert np.allclose(out, dense_out, rtol=1e-12, atol=1e-12) and np.allclose(lse, dense_lse, rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------- sparse prefill
+def _bf16_bits_of(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bits_f64(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double()
+
+
+def test_sparse_prefill_all_rows_is_dense_attention(oracle_lib):
+    """flash_mla_sparse_fwd ("Implementation:Sgl project Sglang Flash MLA", Signature, I/O
+    Contract): with every kv row listed (in any order) the result is dense attention over kv:
+    out and lse against torch float64 SDPA / logsumexp, max_logits against torch's max of the
+    scaled scores."""
+    rng = np.random.default_rng(80)
+    T, N, s_kv = 3, 8, 150
+    q = _bf16_bits_of(rng.standard_normal((T, N, 576)))
+    kv = _bf16_bits_of(rng.standard_normal((s_kv, 576)))
+    idx = np.stack([rng.permutation(s_kv) for _ in range(T)]).astype(np.int32)
+    scale = 1 / math.sqrt(192)
+    out, mx, lse = oracle.sparse_prefill(q, kv, idx, scale)
+    Q, K = _bits_f64(q), _bits_f64(kv)
+    for t in range(T):
+        s = (Q[t] @ K.T) * scale
+        ro = torch.nn.functional.scaled_dot_product_attention(Q[t][:, None], K[None].expand(N, -1, -1),
+                                                              K[None, :, :512].expand(N, -1, -1), scale=scale)[:, 0]
+        assert np.allclose(out[t], ro.numpy(), rtol=0, atol=1e-11)
+        assert np.allclose(lse[t], torch.logsumexp(s, 1).numpy(), rtol=0, atol=1e-11)
+        assert np.allclose(mx[t], s.max(1).values.numpy(), rtol=0, atol=1e-12)
+
+
+def test_sparse_prefill_skips_invalid_and_counts_duplicates(oracle_lib):
+    """Entries outside [0, s_kv) are skipped; a token with none gives out = 0, lse = -inf and
+    max_logits = -inf; a row listed twice adds its weight twice: lse = ln(e^lse1 + e^s_dup)
+    (a closed form of the sum over keys). Invariants: max_logits <= lse <= max_logits + ln(n)."""
+    rng = np.random.default_rng(81)
+    T, N, s_kv, k = 4, 4, 90, 40
+    q = _bf16_bits_of(rng.standard_normal((T, N, 576)))
+    kv = _bf16_bits_of(rng.standard_normal((s_kv, 576)))
+    base = np.stack([rng.choice(s_kv, k, replace=False) for _ in range(T)]).astype(np.int32)
+    scale = 0.05
+    o1, m1, l1 = oracle.sparse_prefill(q, kv, base, scale)
+    noisy = np.concatenate([base, np.full((T, 7), -1, np.int32), np.full((T, 3), s_kv + 5, np.int32)], axis=1)
+    noisy = np.stack([rng.permutation(r) for r in noisy]).astype(np.int32)
+    o2, m2, l2 = oracle.sparse_prefill(q, kv, noisy, scale)
+    assert np.allclose(o1, o2, atol=1e-13) and np.allclose(l1, l2, atol=1e-13) and np.array_equal(m1, m2)
+    empty = np.full((T, 5), -1, np.int32)
+    o3, m3, l3 = oracle.sparse_prefill(q, kv, empty, scale)
+    assert np.all(o3 == 0) and np.all(np.isneginf(l3)) and np.all(np.isneginf(m3))
+    dup = np.concatenate([base, base[:, :1]], axis=1)
+    _, _, l4 = oracle.sparse_prefill(q, kv, dup, scale)
+    Q, K = _bits_f64(q), _bits_f64(kv)
+    for t in range(T):
+        s_dup = ((Q[t] @ K[int(base[t, 0])]) * scale).numpy()
+        assert np.allclose(l4[t], np.logaddexp(l1[t], s_dup), atol=1e-12)
+    assert np.all(m1 <= l1 + 1e-12) and np.all(l1 <= m1 + math.log(k) + 1e-12)

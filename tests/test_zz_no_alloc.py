@@ -5,7 +5,8 @@ whole GPU budget and forbids cudaMalloc by extensions, a latency-critical loop
 that must not pay for an allocation, a language binding without CUDA allocation —
 use this variant, which runs the same decode on a workspace the library keeps
 in a static device array. These tests call it through the C ABI and check it
-against mla_decode with a caller-allocated workspace, on two calls in a row.
+against mla_decode with a caller-allocated workspace, on two calls in a row, and
+the second call's result against the oracle.
 
 The file name sorts last so that a run stopping at the first failure has
 already run every other test.
@@ -18,7 +19,7 @@ import torch
 
 import mla_paged_latent_gb300 as mla
 import workloads
-from gpu_helpers import DeviceWorkload, assert_close
+from gpu_helpers import DeviceWorkload, assert_close, bound_for, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -74,8 +75,12 @@ def test_static_workspace_matches_mla_decode(lib, name):
         assert rc == 0, lib.mla_last_error()
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        assert_close(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ref_out,
-                     ref_lse, f"{name} call {call}")
+        got_out = out.float().cpu().numpy().astype(np.float64)
+        got_lse = lse.cpu().numpy().astype(np.float64)
+        assert_close(got_out, got_lse, ref_out, ref_lse, f"{name} call {call}", bound_for(w.cfg.layout))
+    # and the oracle agrees with the static-workspace result
+    o_out, o_lse = oracle_decode(w)
+    assert_close(got_out, got_lse, o_out, o_lse, f"{name} vs the oracle", bound_for(w.cfg.layout))
 
 
 def test_static_workspace_rejects_oversized_plans(lib):
