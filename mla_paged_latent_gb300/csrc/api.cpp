@@ -260,6 +260,33 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
     if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the KV tensor map failed (%d)", (int)r);
   }
 
+  // whole 64-row blocks in one copy: Q rows x 9 dim slabs, and 9 or 2 dim slabs of a page block
+  mla::WideMaps wide;
+  std::memset(&wide, 0, sizeof wide);
+  if (tma_kv && page_size >= 64 && qbox == 64) {
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    const cuuint64_t qd[3] = {64, static_cast<cuuint64_t>(batch) * R, 9};
+    const cuuint64_t qs[2] = {1152, 128};
+    const cuuint32_t qb[3] = {64, 64, 9};
+    CUresult r = encode(&wide.q9, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qd, qs, qb, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the wide q tensor map failed (%d)", (int)r);
+    const cuuint64_t kd[4] = {64, static_cast<cuuint64_t>(page_size), 9, static_cast<cuuint64_t>(num_pages)};
+    const cuuint64_t ks[3] = {1152, 128, static_cast<cuuint64_t>(page_bytes)};
+    const cuuint32_t kb9[4] = {64, 64, 9, 1};
+    const cuuint32_t kb2[4] = {64, 64, 2, 1};
+    r = encode(&wide.kv9, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), kd, ks, kb9, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the wide KV tensor map failed (%d)", (int)r);
+    r = encode(&wide.kv2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), kd, ks, kb2, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the wide KV tensor map failed (%d)", (int)r);
+    wide.valid = 1;
+  }
+
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t nrows = static_cast<size_t>(total_splits) * static_cast<size_t>(R);
   mla::DecodeParams p;
@@ -308,7 +335,7 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
     int cap = 0;
     if (int rc = pair_cluster_capacity(&cap)) return rc;
     const int work = num_partitions * static_cast<int>(R / 128);
-    e = mla::launch_decode_pair(p, q_map, kv_map, work < cap ? work : cap, s);
+    e = mla::launch_decode_pair(p, q_map, kv_map, wide, work < cap ? work : cap, s);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode: pair decode launch");
   } else {
     mla::DecodeVariant v;

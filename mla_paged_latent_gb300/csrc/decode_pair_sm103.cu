@@ -61,7 +61,7 @@ constexpr uint32_t kOffStage = kOffQ + 9 * kPSlab;       // 2 stages x 9 dim sla
 constexpr uint32_t kStageBytes = 9 * kPSlab;
 constexpr uint32_t kOffP1 = kOffStage + 2 * kStageBytes;  // P of KV rows 64-127 (rows 0-63: the stage's RoPE slab)
 constexpr uint32_t kOffMisc = kOffP1 + kPSlab;
-constexpr uint32_t kPairPrefetchBytes = 224u * 1024u;
+constexpr uint32_t kPairPrefetchBytes = 72u * 1024u;  // one tile: farther ahead thrashes L2 and slows the loads
 constexpr float kPairRescaleLog2 = 32.0f;
 // The S operand's slabs in MMA order, in three groups: the value dims of the even CTA
 // (slabs 0, 1, 4, 5), those of the odd CTA (2, 3, 6, 7), and the RoPE slab (8).
@@ -74,7 +74,7 @@ __device__ __forceinline__ int s_slab(int i) { return 4 * ((i & 3) >> 1) + 2 * (
 enum PairBar {
   // gates of the MMA issuers, arrived on from both CTAs (used in the even CTA)
   kQFull = 0,       // count 2, + bytes
-  kSRegFull = 1,    // + 3 * stage + group (2 x 3): count 2, + bytes
+  kSRegFull = 1,    // + stage (2): count 2, + bytes (slots 3-6 unused)
   kPFull = 7,       // count 8 (the softmax warps of both CTAs)
   kSFree = 8,       // + TMEM buffer (2): count 8
   kOFree = 10,      // count 8
@@ -104,7 +104,7 @@ static_assert(kOffMisc + sizeof(PairMisc) + 1024 <= 232448, "shared memory budge
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     mla_decode_pair_kernel(const __grid_constant__ DecodeParams P, const __grid_constant__ CUtensorMap q_map,
-                           const __grid_constant__ CUtensorMap kv_map) {
+                           const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ WideMaps wide) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_addr(smem);
@@ -123,7 +123,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar(kQFull), 2);
-    for (int g = 0; g < 6; ++g) mbar_init(bar(kSRegFull + g), 2);
+    for (int s = 0; s < 2; ++s) mbar_init(bar(kSRegFull + s), 2);
     mbar_init(bar(kPFull), 8);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kSFree + s), 8);
@@ -188,8 +188,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // Tile t goes to stage t % 2 once the PV of tile t - 2 has released it; each slab group
     // completes on the even CTA's barrier for that group (both CTAs' bytes).
     if (lane == 0) {
-      tma_prefetch_desc(&q_map);
-      tma_prefetch_desc(&kv_map);
+      const bool wide_maps = wide.valid != 0;
+      if (wide_maps) {
+        tma_prefetch_desc(&wide.q9);
+        tma_prefetch_desc(&wide.kv9);
+      } else {
+        tma_prefetch_desc(&q_map);
+        tma_prefetch_desc(&kv_map);
+      }
       int it = 0, u = 0;
       for (int w = cl0; w < num_work && !*abort_flag; w += ncl) {
         const int part = w / PG, g = w % PG;
@@ -198,7 +204,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (u > 0 && !mbar_wait_cluster(bar(kQEmpty), (u - 1) & 1, abort_flag, P.status)) return;
           mbar_arrive_expect_tx_cluster(lead(kQFull), 9 * kPSlab);
           const int row0 = r * R + g * 128 + 64 * c;
-          for (int s = 0; s < 9; ++s) tma_load_2d_pair(sb + kOffQ + s * kPSlab, &q_map, s * 64, row0, lead(kQFull));
+          if (wide_maps) {
+            tma_load_3d_pair(sb + kOffQ, &wide.q9, 0, row0, 0, lead(kQFull));  // all 9 slabs in one copy
+          } else {
+            for (int s = 0; s < 9; ++s) tma_load_2d_pair(sb + kOffQ + s * kPSlab, &q_map, s * 64, row0, lead(kQFull));
+          }
           ++u;
           const int L = request_len(P, r);
           for (int b0 = lo; b0 < hi; b0 += 2, ++it) {
@@ -207,19 +217,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             int pages[8];
             const int own = b0 + c;
             const int nvalid = block_pages(r, own, hi, L, pages);
-            for (int gq = 0; gq < 3; ++gq) {
-              const int n_in = gq < 2 ? 4 : 1;
-              const int gb = kSRegFull + 3 * st + gq;
-              mbar_arrive_expect_tx_cluster(lead(gb), static_cast<uint32_t>(n_in * nvalid * box_rows * 128));
-              for (int i = 0; i < n_in; ++i) {
-                const int s = gq < 2 ? s_slab(4 * gq + i) : 8;
+            mbar_arrive_expect_tx_cluster(lead(kSRegFull + st), static_cast<uint32_t>(9 * nvalid * box_rows * 128));
+            if (wide_maps) {
+              // page_size >= 64: the block is one page run, its 9 slabs one copy
+              if (pages[0] >= 0)
+                tma_load_4d_pair(stage(st), &wide.kv9, 0, (own * kBlockRows) & (P.page_size - 1), 0, pages[0],
+                                 lead(kSRegFull + st));
+            } else {
+              for (int s = 0; s < 9; ++s)
                 for (int k = 0; k < nbox; ++k) {
                   if (pages[k] < 0) continue;
                   const int in_page = (own * kBlockRows + k * box_rows) & (P.page_size - 1);
                   tma_load_3d_pair(stage(st) + s * kPSlab + k * box_rows * 128, &kv_map, s * 64, in_page, pages[k],
-                                   lead(gb));
+                                   lead(kSRegFull + st));
                 }
-              }
             }
             *reinterpret_cast<volatile int*>(&misc->progress) = it + 1;
           }
@@ -229,8 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         // copies still in flight land on this CTA's gates: wait for them (bounded)
         if (u > 0) mbar_wait_drain_cluster(bar(kQFull), (u - 1) & 1);
         for (int k = 1; k <= 2 && it - k >= 0; ++k)
-          for (int gq = 0; gq < 3; ++gq)
-            mbar_wait_drain_cluster(bar(kSRegFull + 3 * ((it - k) & 1) + gq), ((it - k) >> 1) & 1);
+          mbar_wait_drain_cluster(bar(kSRegFull + ((it - k) & 1)), ((it - k) >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -254,14 +264,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             int pages[8];
             const int n = block_pages(r, b0 + h, hi, L, pages);
             mbar_arrive_expect_tx(bar(kVFull + st), 4u * n * box_rows * 128);
-            for (int j = 0; j < 4; ++j) {
-              const int dst_slab = 4 * (j >> 1) + 2 * h + (j & 1);
-              const int src_slab = 4 * (j >> 1) + 2 * c + (j & 1);  // this CTA's value dims
-              for (int k = 0; k < nbox; ++k) {
-                if (pages[k] < 0) continue;
-                const int in_page = ((b0 + h) * kBlockRows + k * box_rows) & (P.page_size - 1);
-                tma_load_3d(stage(st) + dst_slab * kPSlab + k * box_rows * 128, &kv_map, src_slab * 64, in_page,
-                            pages[k], bar(kVFull + st));
+            if (wide.valid) {
+              // two copies of 2 dim slabs each (this CTA's dims of blocks 0 and 1)
+              if (pages[0] >= 0)
+                for (int b = 0; b < 2; ++b)
+                  tma_load_4d(stage(st) + (4 * b + 2 * h) * kPSlab, &wide.kv2, 0,
+                              ((b0 + h) * kBlockRows) & (P.page_size - 1), 4 * b + 2 * c, pages[0], bar(kVFull + st));
+            } else {
+              for (int j = 0; j < 4; ++j) {
+                const int dst_slab = 4 * (j >> 1) + 2 * h + (j & 1);
+                const int src_slab = 4 * (j >> 1) + 2 * c + (j & 1);  // this CTA's value dims
+                for (int k = 0; k < nbox; ++k) {
+                  if (pages[k] < 0) continue;
+                  const int in_page = ((b0 + h) * kBlockRows + k * box_rows) & (P.page_size - 1);
+                  tma_load_3d(stage(st) + dst_slab * kPSlab + k * box_rows * 128, &kv_map, src_slab * 64, in_page,
+                              pages[k], bar(kVFull + st));
+                }
               }
             }
           }
@@ -288,9 +306,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             tc_fence_after();
             const uint32_t d = tmem_s + st * 64;
             const uint64_t ka = kmaj | (stage(st) >> 4);
+            if (!mbar_wait_cluster(bar(kSRegFull + st), (it >> 1) & 1, abort_flag, P.status)) return;
 #pragma unroll 1
             for (int gq = 0; gq < 3; ++gq) {
-              if (!mbar_wait_cluster(bar(kSRegFull + 3 * st + gq), (it >> 1) & 1, abort_flag, P.status)) return;
               const int n_in = gq < 2 ? 4 : 1;
 #pragma unroll 1
               for (int i = 0; i < n_in; ++i) {
@@ -549,21 +567,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ L2 prefetch
-    // Streams this CTA's KV rows of upcoming tiles (and the next units' Q rows) from HBM
-    // into L2, about kPairPrefetchBytes ahead of the S-operand loads, one 128-B line per lane
-    // and instruction through the load/store path: bulk prefetches would occupy the copy
-    // engine that the tensor loads of the operands queue on. A hint only.
+    // Streams this CTA's KV rows of the next tile (and the next units' Q rows) from HBM into
+    // L2 one tile ahead of the S-operand loads: one bulk prefetch per page block (a copy
+    // instruction costs about the same whatever its size). A hint only. Measured on the
+    // 128-head bf16 workload: one tile ahead shortens the S-operand loads by a third; two
+    // tiles ahead gains nothing more, and four or more slow the kernel (L2 thrashing).
     int ahead = static_cast<int>(kPairPrefetchBytes / (static_cast<uint32_t>(kBlockRows) * P.row_bytes));
-    ahead = ahead < 2 ? 2 : ahead;
+    ahead = ahead < 1 ? 1 : ahead;
     int pit = 0;
     for (int w = cl0; w < num_work && !*abort_flag; w += ncl) {
       const int part = w / PG, g = w % PG;
       for_each_unit(P, part, [&](int r, int lo, int hi, int) {
         if (*abort_flag) return;
-        {
-          const uint8_t* qrows = reinterpret_cast<const uint8_t*>(P.q + (static_cast<int64_t>(r) * R + g * 128 + 64 * c) * 576);
-          for (int k = lane; k < 64 * 576 * 2 / 128; k += 32) prefetch_l2_line(qrows + k * 128);
-        }
+        if (lane == 0)
+          prefetch_l2_bulk(P.q + (static_cast<int64_t>(r) * R + g * 128 + 64 * c) * 576, 64u * 576u * 2u);
         const int L = request_len(P, r);
         for (int b0 = lo; b0 < hi; b0 += 2, ++pit) {
           const uint64_t t0 = globaltimer();
@@ -573,19 +590,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             __nanosleep(256);
           }
           const int own = b0 + c;
-          if (own >= hi) continue;
-          for (int k = 0; k < nbox; ++k) {
-            const int pos0 = own * kBlockRows + k * box_rows;
-            if (pos0 >= L) break;
-            const int pi = pos0 >> P.log2_ps;
-            const int page = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
-            if (page < 0 || page >= P.num_pages) continue;
-            const int rows = (L - pos0) < box_rows ? (L - pos0) : box_rows;
-            const uint8_t* src = P.kv + static_cast<int64_t>(page) * P.page_bytes +
-                                 static_cast<int64_t>(pos0 & (P.page_size - 1)) * P.row_bytes;
-            const int lines = (rows * P.row_bytes) >> 7;  // 1152-B rows: 9 lines each
-            for (int i = lane; i < lines; i += 32) prefetch_l2_line(src + i * 128);
-          }
+          if (own >= hi || lane >= nbox) continue;
+          const int pos0 = own * kBlockRows + lane * box_rows;
+          if (pos0 >= L) continue;
+          const int pi = pos0 >> P.log2_ps;
+          const int page = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
+          if (page < 0 || page >= P.num_pages) continue;
+          const int rows = (L - pos0) < box_rows ? (L - pos0) : box_rows;
+          prefetch_l2_bulk(P.kv + static_cast<int64_t>(page) * P.page_bytes +
+                               static_cast<int64_t>(pos0 & (P.page_size - 1)) * P.row_bytes,
+                           static_cast<uint32_t>(rows * P.row_bytes));
         }
       });
     }
@@ -602,13 +616,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 
 size_t decode_pair_smem_bytes() { return kOffMisc + sizeof(PairMisc) + 1024; }
 
-cudaError_t launch_decode_pair(const DecodeParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map, int clusters,
-                               cudaStream_t stream) {
+cudaError_t launch_decode_pair(const DecodeParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
+                               const WideMaps& wide, int clusters, cudaStream_t stream) {
   auto kern = mla_decode_pair_kernel;
   const size_t smem = decode_pair_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(2 * clusters), dim3(kPairThreads), smem, stream, p, q_map, kv_map);
+  return launch_pdl(kern, dim3(2 * clusters), dim3(kPairThreads), smem, stream, p, q_map, kv_map, wide);
 }
 
 cudaError_t decode_pair_max_clusters(int* clusters) {

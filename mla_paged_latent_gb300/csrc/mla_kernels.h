@@ -50,6 +50,18 @@ struct DecodeParams {
   int32_t uniform_len;            // rows of every request when seqlens is null
 };
 
+// Tensor maps that move whole 64-row blocks in one copy (a tensor copy costs about the same
+// issue time whatever its size, so few large copies beat many 8-KiB slabs): q9 = 64 query
+// rows x the 9 dim slabs of a bf16 576-wide row, landing slab-major; kv9 / kv2 = 9 / 2 dim
+// slabs of one 64-row page block. Only encoded (valid) when page_size >= 64 and the
+// request has >= 64 query rows.
+struct WideMaps {
+  CUtensorMap q9;
+  CUtensorMap kv9;
+  CUtensorMap kv2;
+  int valid;
+};
+
 // Kernel variants: layout 0 with TMA page loads (dense), layout 0 gathered by
 // the converter warps (sparse), layouts 1 and 2 (fp8, dense or sparse).
 enum class DecodeVariant { kBf16Tma = 0, kBf16Gather = 1, kFp8_448 = 2, kFp8_512 = 3 };
@@ -60,7 +72,7 @@ size_t decode_smem_bytes(DecodeVariant v);
 // groups of 128 (rows_per_req % 128 == 0); `clusters` pairs of CTAs.
 size_t decode_pair_smem_bytes();
 cudaError_t launch_decode_pair(const DecodeParams& p, const CUtensorMap& q_map, const CUtensorMap& kv_map,
-                               int clusters, cudaStream_t stream);
+                               const WideMaps& wide, int clusters, cudaStream_t stream);
 cudaError_t decode_pair_max_clusters(int* clusters);
 cudaError_t launch_decode(DecodeVariant v, const DecodeParams& p, const CUtensorMap& q_map,
                           const CUtensorMap& kv_map, int grid, cudaStream_t stream);
