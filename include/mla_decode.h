@@ -76,10 +76,12 @@ typedef enum {
 #define MLA_GROUP_ROWS 64       /* query rows (token x head) per CTA work item */
 #define MLA_WORKSPACE_HEADER 256
 #define MLA_DECODE_SKIP_COMBINE 1u  /* mla_decode flag: leave split partials in the workspace */
-/* mla_decode flag: run a bf16 decode whose query rows come in groups of 128 (for example
- * 128 heads) on the CTA-pair kernel, two SMs per group of 128 query rows, instead of the
- * single-SM kernel (same results within the stated tolerances). Ignored for other decodes. */
-#define MLA_DECODE_CTA_PAIR 2u
+/* A dense bf16 decode whose query rows per request (q_tokens_per_req x num_heads) come in
+ * groups of 128 (for example 128 heads) runs on the CTA-pair kernel: two SMs per group of
+ * 128 query rows share each KV tile through one tensor-core pair. mla_decode flag: run it on
+ * the single-SM kernel instead (same results within the stated tolerances; for comparison
+ * and testing). Ignored for other decodes. */
+#define MLA_DECODE_SINGLE_SM 2u
 /* mla_decode flag, for testing failure detection only: the decode kernel withholds
  * the signal that its first score tile is complete, so the softmax's bounded wait
  * runs out; every role then leaves its loop, the call completes, and the workspace

@@ -163,12 +163,13 @@ def mla_decode_plan(cache_seqlens, q_tokens_per_req: int, num_heads: int, topk: 
 def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seqlens, q_tokens_per_req: int,
                sm_scale: float, sched, num_splits, num_partitions: int, total_splits: int, workspace, out, lse,
                sink=None, indices=None, causal: bool = False, skip_combine: bool = False, stream=None,
-               cta_pair: bool = False, _test_withhold_signal: bool = False):
+               single_sm: bool = False, _test_withhold_signal: bool = False):
     """Enqueue decode (+ split combine) on `stream`. All tensors on the GPU:
     q bf16 [T, N, Dqk]; kv_cache uint8 [num_pages, page_bytes]; block_table int32 [B, max_pages];
     cache_seqlens int32 [B]; sched int32 [P, 8]; num_splits int32 [B+1]; workspace uint8;
     out bf16 [T, N, 512]; lse float32 [T, N]; sink float32 [N] or None; indices int32 [T, topk] or None.
-    cta_pair: run a bf16 decode whose query rows come in groups of 128 on the CTA-pair kernel."""
+    single_sm: run a dense bf16 decode whose query rows come in groups of 128 on the single-SM
+    kernel instead of the CTA-pair kernel."""
     _require_cuda(q, kv_cache, block_table, cache_seqlens, sched, num_splits, workspace, out, lse, sink, indices)
     T, N, D = q.shape
     B = cache_seqlens.shape[0]
@@ -177,7 +178,7 @@ def mla_decode(q, kv_cache, layout: int, page_size: int, block_table, cache_seql
                              block_table.shape[1], _ptr(cache_seqlens), B, q_tokens_per_req, N, float(sm_scale),
                              _ptr(sink), _ptr(indices), topk, int(bool(causal)), _ptr(sched), _ptr(num_splits),
                              num_partitions, total_splits, _ptr(workspace), workspace.numel(), _ptr(out), _ptr(lse),
-                             (1 if skip_combine else 0) | (2 if cta_pair else 0) |
+                             (1 if skip_combine else 0) | (2 if single_sm else 0) |
                              (0x80000000 if _test_withhold_signal else 0),
                              _stream(stream)))
 

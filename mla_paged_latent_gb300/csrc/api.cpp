@@ -260,7 +260,7 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
     if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the KV tensor map failed (%d)", (int)r);
   }
 
-  // whole 64-row blocks in one copy: Q rows x 9 dim slabs, and 9 or 2 dim slabs of a page block
+  // whole 64-row blocks in few copies: Q rows x 9 dim slabs, and 3 or 2 dim slabs of a page block
   mla::WideMaps wide;
   std::memset(&wide, 0, sizeof wide);
   if (tma_kv && page_size >= 64 && qbox == 64) {
@@ -274,9 +274,9 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
     if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the wide q tensor map failed (%d)", (int)r);
     const cuuint64_t kd[4] = {64, static_cast<cuuint64_t>(page_size), 9, static_cast<cuuint64_t>(num_pages)};
     const cuuint64_t ks[3] = {1152, 128, static_cast<cuuint64_t>(page_bytes)};
-    const cuuint32_t kb9[4] = {64, 64, 9, 1};
+    const cuuint32_t kb3[4] = {64, 64, 3, 1};
     const cuuint32_t kb2[4] = {64, 64, 2, 1};
-    r = encode(&wide.kv9, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), kd, ks, kb9, es,
+    r = encode(&wide.kv3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(kv_cache), kd, ks, kb3, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "mla_decode: encoding the wide KV tensor map failed (%d)", (int)r);
@@ -330,7 +330,7 @@ int decode_impl(const void* q, const void* kv_cache, mla_kv_layout layout, int64
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (tma_kv && R % 128 == 0 && (flags & MLA_DECODE_CTA_PAIR)) {
+  if (tma_kv && R % 128 == 0 && !(flags & MLA_DECODE_SINGLE_SM)) {
     // query rows in groups of 128: one CTA pair per (partition, group of 128 rows)
     int cap = 0;
     if (int rc = pair_cluster_capacity(&cap)) return rc;

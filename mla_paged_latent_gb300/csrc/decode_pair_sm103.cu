@@ -36,14 +36,16 @@
 // needs; P of rows 64-127 to the extra slab. Tile t+1 loads into the other stage while tile
 // t is computed.
 //
-// Warp roles (288 threads):
+// Warp roles (416 threads):
 //   warp 0      TMA: Q once per unit and the S operand (completion counted on the even
 //               CTA's barriers, which gate the MMAs)
 //   warp 1      TMEM allocation; TMA of the V operand (local barrier)
 //   warp 2      S MMA issuer (even CTA only)
 //   warp 3      PV MMA issuer (even CTA only)
-//   warps 4-7   softmax (lane r + 64h: query row r over tile half h), O rescale, epilogue
-//   warp 8      L2 prefetch of this CTA's upcoming KV rows
+//   warps 4-11  softmax (lane r + 64h: query row r over tile half h; warps 4-7 take S
+//               columns 0-31 and O block 0, warps 8-11 columns 32-63 and O block 1),
+//               O rescale, epilogue
+//   warp 12     L2 prefetch of this CTA's upcoming KV rows
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -54,7 +56,7 @@
 namespace mla {
 namespace {
 
-constexpr int kPairThreads = 288;
+constexpr int kPairThreads = 416;
 constexpr uint32_t kPSlab = 8192;  // 64 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffStage = kOffQ + 9 * kPSlab;       // 2 stages x 9 dim slabs of the tile's KV rows
@@ -63,10 +65,11 @@ constexpr uint32_t kOffP1 = kOffStage + 2 * kStageBytes;  // P of KV rows 64-127
 constexpr uint32_t kOffMisc = kOffP1 + kPSlab;
 constexpr uint32_t kPairPrefetchBytes = 72u * 1024u;  // one tile: farther ahead thrashes L2 and slows the loads
 constexpr float kPairRescaleLog2 = 32.0f;
-// The S operand's slabs in MMA order, in three groups: the value dims of the even CTA
-// (slabs 0, 1, 4, 5), those of the odd CTA (2, 3, 6, 7), and the RoPE slab (8).
-// Slab i of groups 0 and 1 (i = 4 g + m): 4 (m >> 1) + 2 g + (m & 1).
-__device__ __forceinline__ int s_slab(int i) { return 4 * ((i & 3) >> 1) + 2 * (i >> 2) + (i & 1); }
+// A stage arrives in three parts of three dim slabs (slabs 3p .. 3p + 2), each on its own
+// barrier, so that the S MMAs of the first slabs run while the later ones are still landing.
+// S reads the slabs in order; the value slabs 4b + 2h + {0, 1} (block b, CTA h's dims) are
+// released to the reload as a pair once slab 4b + 2h + 1 has been read.
+constexpr int kStageParts = 3;
 
 // Every barrier whose arrivals for tile t + 1 could come before its waiter has seen tile t
 // is kept per stage (or per TMEM buffer): a parity wait must never be more than one phase
@@ -74,21 +77,21 @@ __device__ __forceinline__ int s_slab(int i) { return 4 * ((i & 3) >> 1) + 2 * (
 enum PairBar {
   // gates of the MMA issuers, arrived on from both CTAs (used in the even CTA)
   kQFull = 0,       // count 2, + bytes
-  kSRegFull = 1,    // + stage (2): count 2, + bytes (slots 3-6 unused)
-  kPFull = 7,       // count 8 (the softmax warps of both CTAs)
-  kSFree = 8,       // + TMEM buffer (2): count 8
-  kOFree = 10,      // count 8
+  kSRegFull = 1,    // + 3 * stage + part (2 x 3): count 2, + bytes
+  kPFull = 7,       // count 16 (the softmax warps of both CTAs)
+  kSFree = 8,       // + TMEM buffer (2): count 16
+  kOFree = 10,      // count 16
   // signalled in both CTAs by the even CTA's multicast commits
   kSFull = 11,      // + TMEM buffer (2)
-  kSDone = 13,      // + 2 * stage + value-dim group (2 x 2): S has read those slabs of the stage
-  kStageFree = 17,  // + stage (2): the PV of the stage's tile has completed
-  kPvDone = 19,
-  kQEmpty = 20,
-  kOFull = 21,
+  kSDone = 13,      // + 4 * stage + 2 * b + h (2 x 4): S has read the slabs 4b + 2h + {0, 1}
+  kStageFree = 21,  // + stage (2): the PV of the stage's tile has completed
+  kPvDone = 23,
+  kQEmpty = 24,
+  kOFull = 25,
   // local to each CTA
-  kVFull = 22,      // + stage (2): count 1, + bytes: this CTA's reload of the peer rows' values
-  kFinal = 24,      // count 2: the last commit of each issuer (even CTA)
-  kNumPairBars = 25
+  kVFull = 26,      // + stage (2): count 1, + bytes: this CTA's reload of the peer rows' values
+  kFinal = 28,      // count 2: the last commit of each issuer (even CTA)
+  kNumPairBars = 29
 };
 
 struct PairMisc {
@@ -97,8 +100,9 @@ struct PairMisc {
   int abort;
   int progress;  // tiles whose S operand loads have been issued (throttles the L2 prefetch)
   int pad;
-  float xmax[128];  // tile maxima of the two lanes of a query row (slow path only)
-  float xl[128];    // partial sums of the two lanes of a query row (end of a unit)
+  // the four threads of a query row exchange their tile maxima (slow path of a tile) and,
+  // at the end of a unit, their partial sums here
+  float xchg[256];
 };
 static_assert(kOffMisc + sizeof(PairMisc) + 1024 <= 232448, "shared memory budget of one CTA");
 
@@ -123,16 +127,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar(kQFull), 2);
-    for (int s = 0; s < 2; ++s) mbar_init(bar(kSRegFull + s), 2);
-    mbar_init(bar(kPFull), 8);
+    for (int s = 0; s < 2 * kStageParts; ++s) mbar_init(bar(kSRegFull + s), 2);
+    mbar_init(bar(kPFull), 16);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(kSFree + s), 8);
+      mbar_init(bar(kSFree + s), 16);
       mbar_init(bar(kSFull + s), 1);
       mbar_init(bar(kStageFree + s), 1);
       mbar_init(bar(kVFull + s), 1);
-      for (int g = 0; g < 2; ++g) mbar_init(bar(kSDone + 2 * s + g), 1);
+      for (int g = 0; g < 4; ++g) mbar_init(bar(kSDone + 4 * s + g), 1);
     }
-    mbar_init(bar(kOFree), 8);
+    mbar_init(bar(kOFree), 16);
     mbar_init(bar(kPvDone), 1);
     mbar_init(bar(kQEmpty), 1);
     mbar_init(bar(kOFull), 1);
@@ -191,7 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const bool wide_maps = wide.valid != 0;
       if (wide_maps) {
         tma_prefetch_desc(&wide.q9);
-        tma_prefetch_desc(&wide.kv9);
+        tma_prefetch_desc(&wide.kv3);
       } else {
         tma_prefetch_desc(&q_map);
         tma_prefetch_desc(&kv_map);
@@ -217,19 +221,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             int pages[8];
             const int own = b0 + c;
             const int nvalid = block_pages(r, own, hi, L, pages);
-            mbar_arrive_expect_tx_cluster(lead(kSRegFull + st), static_cast<uint32_t>(9 * nvalid * box_rows * 128));
+            for (int pt = 0; pt < kStageParts; ++pt)
+              mbar_arrive_expect_tx_cluster(lead(kSRegFull + kStageParts * st + pt),
+                                            static_cast<uint32_t>(3 * nvalid * box_rows * 128));
             if (wide_maps) {
-              // page_size >= 64: the block is one page run, its 9 slabs one copy
+              // page_size >= 64: the block is one page run, each part of 3 slabs one copy
               if (pages[0] >= 0)
-                tma_load_4d_pair(stage(st), &wide.kv9, 0, (own * kBlockRows) & (P.page_size - 1), 0, pages[0],
-                                 lead(kSRegFull + st));
+                for (int pt = 0; pt < kStageParts; ++pt)
+                  tma_load_4d_pair(stage(st) + 3 * pt * kPSlab, &wide.kv3, 0, (own * kBlockRows) & (P.page_size - 1),
+                                   3 * pt, pages[0], lead(kSRegFull + kStageParts * st + pt));
             } else {
               for (int s = 0; s < 9; ++s)
                 for (int k = 0; k < nbox; ++k) {
                   if (pages[k] < 0) continue;
                   const int in_page = (own * kBlockRows + k * box_rows) & (P.page_size - 1);
                   tma_load_3d_pair(stage(st) + s * kPSlab + k * box_rows * 128, &kv_map, s * 64, in_page, pages[k],
-                                   lead(kSRegFull + st));
+                                   lead(kSRegFull + kStageParts * st + s / 3));
                 }
             }
             *reinterpret_cast<volatile int*>(&misc->progress) = it + 1;
@@ -240,7 +247,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         // copies still in flight land on this CTA's gates: wait for them (bounded)
         if (u > 0) mbar_wait_drain_cluster(bar(kQFull), (u - 1) & 1);
         for (int k = 1; k <= 2 && it - k >= 0; ++k)
-          mbar_wait_drain_cluster(bar(kSRegFull + ((it - k) & 1)), ((it - k) >> 1) & 1);
+          for (int pt = 0; pt < kStageParts; ++pt)
+            mbar_wait_drain_cluster(bar(kSRegFull + kStageParts * ((it - k) & 1) + pt), ((it - k) >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -260,25 +268,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           for (int b0 = lo; b0 < hi; b0 += 2, ++it) {
             const int st = it & 1;
             const int h = 1 - c;  // the peer's half
-            if (!mbar_wait_cluster(bar(kSDone + 2 * st + h), (it >> 1) & 1, abort_flag, P.status)) return;
             int pages[8];
-            const int n = block_pages(r, b0 + h, hi, L, pages);
-            mbar_arrive_expect_tx(bar(kVFull + st), 4u * n * box_rows * 128);
-            if (wide.valid) {
-              // two copies of 2 dim slabs each (this CTA's dims of blocks 0 and 1)
-              if (pages[0] >= 0)
-                for (int b = 0; b < 2; ++b)
+            for (int b = 0; b < 2; ++b) {
+              // the slabs 4b + 2h + {0, 1} are free once S has read them
+              if (!mbar_wait_cluster(bar(kSDone + 4 * st + 2 * b + h), (it >> 1) & 1, abort_flag, P.status)) return;
+              if (b == 0) {
+                // (only now: S of this tile has begun, so the stage's previous reload has landed
+                // and been waited for, and this arrival opens the barrier's next phase)
+                const int n = block_pages(r, b0 + h, hi, L, pages);
+                mbar_arrive_expect_tx(bar(kVFull + st), 4u * n * box_rows * 128);
+              }
+              if (wide.valid) {
+                // one copy of 2 dim slabs: this CTA's dims of block b
+                if (pages[0] >= 0)
                   tma_load_4d(stage(st) + (4 * b + 2 * h) * kPSlab, &wide.kv2, 0,
                               ((b0 + h) * kBlockRows) & (P.page_size - 1), 4 * b + 2 * c, pages[0], bar(kVFull + st));
-            } else {
-              for (int j = 0; j < 4; ++j) {
-                const int dst_slab = 4 * (j >> 1) + 2 * h + (j & 1);
-                const int src_slab = 4 * (j >> 1) + 2 * c + (j & 1);  // this CTA's value dims
-                for (int k = 0; k < nbox; ++k) {
-                  if (pages[k] < 0) continue;
-                  const int in_page = ((b0 + h) * kBlockRows + k * box_rows) & (P.page_size - 1);
-                  tma_load_3d(stage(st) + dst_slab * kPSlab + k * box_rows * 128, &kv_map, src_slab * 64, in_page,
-                              pages[k], bar(kVFull + st));
+              } else {
+                for (int j = 0; j < 2; ++j) {
+                  const int dst_slab = 4 * b + 2 * h + j;
+                  const int src_slab = 4 * b + 2 * c + j;  // this CTA's value dims
+                  for (int k = 0; k < nbox; ++k) {
+                    if (pages[k] < 0) continue;
+                    const int in_page = ((b0 + h) * kBlockRows + k * box_rows) & (P.page_size - 1);
+                    tma_load_3d(stage(st) + dst_slab * kPSlab + k * box_rows * 128, &kv_map, src_slab * 64, in_page,
+                                pages[k], bar(kVFull + st));
+                  }
                 }
               }
             }
@@ -306,20 +320,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             tc_fence_after();
             const uint32_t d = tmem_s + st * 64;
             const uint64_t ka = kmaj | (stage(st) >> 4);
-            if (!mbar_wait_cluster(bar(kSRegFull + st), (it >> 1) & 1, abort_flag, P.status)) return;
-#pragma unroll 1
-            for (int gq = 0; gq < 3; ++gq) {
-              const int n_in = gq < 2 ? 4 : 1;
-#pragma unroll 1
-              for (int i = 0; i < n_in; ++i) {
-                const int s = gq < 2 ? s_slab(4 * gq + i) : 8;
+            // Fully unrolled, so that the descriptors are the base plus constants: an MMA issued
+            // from a loop that computes its descriptors costs about 70 cycles, unrolled about 50.
+#pragma unroll
+            for (int pt = 0; pt < kStageParts; ++pt) {
+              if (!mbar_wait_cluster(bar(kSRegFull + kStageParts * st + pt), (it >> 1) & 1, abort_flag, P.status))
+                return;
+              tc_fence_after();
+#pragma unroll
+              for (int i = 0; i < 3; ++i) {
+                const int s = 3 * pt + i;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                   mma_bf16_pair(d, qa + s * (kPSlab >> 4) + kk * 2, ka + s * (kPSlab >> 4) + kk * 2, idesc_s,
-                                (gq | i | kk) ? 1u : 0u);
+                                (s | kk) ? 1u : 0u);
+                // value slabs 4b + 2h + {0, 1} read: the reloader may overwrite them
+                if (s < 8 && (s & 1)) mma_commit_pair(bar(kSDone + 4 * st + (s >> 1)), 3);
               }
-              // the value-dim slabs of a CTA may now be reloaded by the other CTA's reloader
-              if (gq < 2) mma_commit_pair(bar(kSDone + 2 * st + gq), 3);
             }
             // (failure-detection test: withhold the first tile's signal so that the
             // softmax's bounded wait runs out)
@@ -352,7 +369,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             tc_fence_after();
             const uint64_t p0 = kmaj | ((stage(st) + 8 * kPSlab) >> 4);  // P of KV rows 0-63: the RoPE slab
             const uint64_t vb = vmaj | (stage(st) >> 4);
-#pragma unroll 1
+#pragma unroll
             for (int b = 0; b < 2; ++b) {
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
@@ -372,14 +389,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       mma_commit_pair(bar(kFinal), 1);
       mbar_wait_drain_cluster(bar(kFinal), 0);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax / epilogue
     // Lane wt = r + 64h of TMEM holds query row r (of this CTA's 64) against KV tile half
-    // h in S, and dims 256b + 128h + 0..127 of that row in O. The two lanes of a row meet
-    // through shared memory; the four warps meet at named barrier 1 (no time limit: a
-    // thread whose bounded wait fails marks itself dead and all stop together at the
-    // next barrier).
-    const int wt = tid - 128;
+    // h in S, and dims 256b + 128h + 0..127 of that row in O. Two warps share each
+    // 32-lane quarter (a warp reaches the lanes 32 (warp % 4) .. + 31): column group
+    // cg = 0 takes S columns 0-31 and O block 0, cg = 1 columns 32-63 and O block 1. The
+    // four threads of a row meet through shared memory; the eight warps meet at named
+    // barrier 1 (no time limit: a thread whose bounded wait fails marks itself dead and
+    // all stop together at the next barrier).
+    const int sx = tid - 128;  // 0 .. 255
+    const int cg = sx >> 7;
+    const int wt = sx & 127;
     const int r = wt & 63;
     const int half = wt >> 6;
     const uint32_t lane_off = static_cast<uint32_t>(wt & ~31) << 16;
@@ -408,51 +429,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         for (int b0 = lo; b0 < hi; b0 += 2, ++it) {
           const int st = it & 1;
           const bool first = b0 == lo;
-          uint32_t sr[64];
+          uint32_t sr[32];
           wait(bar(kSFull + st), (it >> 1) & 1);
           if (!dead) {
             tc_fence_after();
-            tmem_ld32(tmem_s + st * 64 + lane_off, sr);
-            tmem_ld32(tmem_s + st * 64 + lane_off + 32, sr + 32);
+            tmem_ld32(tmem_s + st * 64 + lane_off + cg * 32, sr);
             tmem_wait_ld();
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(lead(kSFree + st));
-          const int pos0 = (b0 + half) * kBlockRows;
+          const int pos0 = (b0 + half) * kBlockRows + cg * 32;  // KV position of this thread's column 0
           int nv = row_end - pos0;
-          nv = nv < 0 ? 0 : (nv > 64 ? 64 : nv);
-          const uint64_t vmask = nv == 64 ? ~0ull : ((1ull << nv) - 1ull);
-          float x[64];
+          nv = nv < 0 ? 0 : (nv > 32 ? 32 : nv);
+          const uint32_t vmask = nv == 32 ? ~0u : ((1u << nv) - 1u);
+          float x[32];
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int cc = 0; cc < 64; ++cc) {
-            x[cc] = ((vmask >> cc) & 1ull) ? __uint_as_float(sr[cc]) : -INFINITY;
+          for (int cc = 0; cc < 32; ++cc) {
+            x[cc] = ((vmask >> cc) & 1u) ? __uint_as_float(sr[cc]) : -INFINITY;
             m4[cc & 3] = fmaxf(m4[cc & 3], x[cc]);
           }
           const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
           // the running maximum of a row moves (lazily) only when a tile exceeds it by more
-          // than kPairRescaleLog2 powers of two; both lanes of the row take the same decision
+          // than kPairRescaleLog2 powers of two; the four threads of the row take the same
+          // decision
           const bool raise = mt > m_run + kPairRescaleLog2;
           float m_new = m_run;
-          const bool any = named_bar_or(1, 128, raise || dead);
+          const bool any = named_bar_or(1, 256, raise || dead);
           if (any) {
-            if (named_bar_or(1, 128, dead)) {
+            if (named_bar_or(1, 256, dead)) {
               stop = true;
               return;
             }
-            misc->xmax[wt] = mt;
-            named_bar_sync(1, 128);
-            const float mh = fmaxf(mt, misc->xmax[wt ^ 64]);
+            misc->xchg[sx] = mt;
+            named_bar_sync(1, 256);
+            const float mh = fmaxf(fmaxf(misc->xchg[r], misc->xchg[r + 64]),
+                                   fmaxf(misc->xchg[128 + r], misc->xchg[128 + r + 64]));
             m_new = (mh > m_run + kPairRescaleLog2) ? mh : m_run;
           }
           const bool rescale = any && !first && m_new != m_run && m_run != -INFINITY;
           const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
           const float alpha = fast_exp2(m_run - m_use);
           float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
+          for (int cc = 0; cc < 16; ++cc) {
             const float p0 = fast_exp2(fmaf(x[2 * cc], P.scale_log2, -m_use));
             const float p1 = fast_exp2(fmaf(x[2 * cc + 1], P.scale_log2, -m_use));
             ps4[cc & 3] += p0 + p1;
@@ -463,13 +485,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           // P of KV rows 64-127 and O belong to the previous tile's PV until it completes
           if (it > 0) wait(bar(kPvDone), (it - 1) & 1);
           if (any && !first && !dead) {
-            // one TMEM round trip per 32 columns of this lane's 256 O columns
+            // one TMEM round trip per 32 columns of this thread's 128 O columns
             tc_fence_after();
             const float a = rescale ? alpha : 1.0f;
 #pragma unroll 1
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 4; ++k) {
               uint32_t t32[32];
-              const uint32_t ta = tmem_o + lane_off + k * 32;
+              const uint32_t ta = tmem_o + lane_off + cg * 128 + k * 32;
               tmem_ld32(ta, t32);
               tmem_wait_ld();
 #pragma unroll
@@ -480,12 +502,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             tc_fence_before();
           }
           if (!dead) {
-            // P row r: KV rows of tile half `half`, 64 bf16 along K (K-major, 128-B swizzle);
-            // half 0 goes to the stage's RoPE slab, which S has finished with
+            // P row r: KV rows of tile half `half`, 64 bf16 along K (K-major, 128-B swizzle),
+            // of which this thread holds the 16-B chunks 4 cg .. 4 cg + 3; half 0 goes to the
+            // stage's RoPE slab, which S has finished with
             const uint32_t pa = (half ? sb + kOffP1 : stage(st) + 8 * kPSlab) + r * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-              st_shared_v4(pa + ((c8 ^ (r & 7)) << 4), make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]));
+            for (int q4 = 0; q4 < 4; ++q4)
+              st_shared_v4(pa + (((4 * cg + q4) ^ (r & 7)) << 4),
+                           make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]));
           }
           // the peer rows' values of this CTA's dims have landed; rows past the loaded range may
           // hold stale or non-finite bytes: zero them (their P is 0, and 0 x NaN would not be)
@@ -495,7 +519,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
               int z0 = v_end - (b0 + hh) * kBlockRows;
               z0 = z0 < 0 ? 0 : z0;
               const int nz = (kBlockRows - z0) * 4 * 8;  // rows x slabs x 16-B chunks
-              for (int idx = wt; idx < nz; idx += 128) {
+              for (int idx = sx; idx < nz; idx += 256) {
                 const int rr = z0 + idx / 32;
                 const int j = (idx >> 3) & 3;
                 const int ch = idx & 7;
@@ -509,12 +533,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (lane == 0 && !dead) mbar_arrive_cluster(lead(kPFull));
         }
         // -------------------------------------------------------- epilogue
-        misc->xl[wt] = l_run;
-        if (named_bar_or(1, 128, dead)) {
+        named_bar_sync(1, 256);  // every thread has read the last tile's maxima
+        misc->xchg[sx] = l_run;
+        if (named_bar_or(1, 256, dead)) {
           stop = true;
           return;
         }
-        const float l_tot = misc->xl[r] + misc->xl[r + 64];
+        const float l_tot = (misc->xchg[r] + misc->xchg[r + 64]) + (misc->xchg[128 + r] + misc->xchg[128 + r + 64]);
         const int base_split = P.num_splits[rq];
         const int nsplit = P.num_splits[rq + 1] - base_split;
         const int sg = base_split + sidx;
@@ -525,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           inv = 1.0f / denom;
           lse2 = m_run + log2f(l_tot);
         }
-        if (half == 0) {
+        if (half == 0 && cg == 0) {
           const float lse_nat = lse2 * 0.6931471805599453f;
           if (nsplit == 1) P.lse[(int64_t)rq * R + grow] = lse_nat;
           else P.part_lse[(int64_t)sg * R + grow] = lse_nat;
@@ -534,11 +559,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           tc_fence_after();
           const int64_t orow = (nsplit == 1 ? (int64_t)rq : (int64_t)sg) * R + grow;
 #pragma unroll 1
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 4; ++k) {
             uint32_t t32[32];
-            tmem_ld32(tmem_o + lane_off + k * 32, t32);
+            tmem_ld32(tmem_o + lane_off + cg * 128 + k * 32, t32);
             tmem_wait_ld();
-            const int d0 = (k >> 2) * 256 + half * 128 + (k & 3) * 32;  // first value dim of these 32 columns
+            const int d0 = cg * 256 + half * 128 + k * 32;  // first value dim of these 32 columns
             if (nsplit == 1) {
               uint4* o = reinterpret_cast<uint4*>(P.out + orow * 512 + d0);
 #pragma unroll
@@ -565,7 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         ++u;
       });
     }
-  } else if (warp == 8) {
+  } else if (warp == 12) {
     // ------------------------------------------------------------ L2 prefetch
     // Streams this CTA's KV rows of the next tile (and the next units' Q rows) from HBM into
     // L2 one tile ahead of the S-operand loads: one bulk prefetch per page block (a copy

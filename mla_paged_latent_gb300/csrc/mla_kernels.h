@@ -52,12 +52,12 @@ struct DecodeParams {
 
 // Tensor maps that move whole 64-row blocks in one copy (a tensor copy costs about the same
 // issue time whatever its size, so few large copies beat many 8-KiB slabs): q9 = 64 query
-// rows x the 9 dim slabs of a bf16 576-wide row, landing slab-major; kv9 / kv2 = 9 / 2 dim
+// rows x the 9 dim slabs of a bf16 576-wide row, landing slab-major; kv3 / kv2 = 3 / 2 dim
 // slabs of one 64-row page block. Only encoded (valid) when page_size >= 64 and the
 // request has >= 64 query rows.
 struct WideMaps {
   CUtensorMap q9;
-  CUtensorMap kv9;
+  CUtensorMap kv3;
   CUtensorMap kv2;
   int valid;
 };

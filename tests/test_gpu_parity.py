@@ -509,9 +509,9 @@ PAIR_CASES = ["dsv3_small", "verify_small", "dsv3_ps16", "dsv3_ps8", "verify_sq2
 @pytest.mark.parametrize("name", PAIR_CASES)
 @pytest.mark.parametrize("min_splits", [1, 5])
 def test_decode_pair_and_single_sm_kernels(name, min_splits):
-    """bf16 decodes whose query rows come in groups of 128 run on the single-SM kernel or,
-    with MLA_DECODE_CTA_PAIR, on CTA pairs: both must agree with the oracle on the same
-    plans."""
+    """bf16 decodes whose query rows come in groups of 128 run on CTA pairs or, with
+    MLA_DECODE_SINGLE_SM, on the single-SM kernel: both must agree with the oracle on the
+    same plans."""
     w = workloads.generate(SMALL[name]())
     assert (w.cfg.sq * w.cfg.heads) % 128 == 0 and w.cfg.layout == 0
     d = DeviceWorkload(w)
@@ -523,7 +523,7 @@ def test_decode_pair_and_single_sm_kernels(name, min_splits):
         d.out.fill_(float("nan"))
         mla.mla_decode(d.q, d.kv, c.layout, c.page_size, d.bt, d.sl, c.sq, c.sm_scale, d.sched, d.ns,
                        d.plan.num_partitions, d.plan.total_splits, d.ws, d.out, d.lse, causal=c.causal,
-                       cta_pair=not single)
+                       single_sm=single)
         assert mla.mla_read_status(d.ws) == 0
         out = d.out.float().cpu().numpy().astype(np.float64)
         lse = d.lse.cpu().numpy().astype(np.float64)
