@@ -36,16 +36,15 @@
 // needs; P of rows 64-127 to the extra slab. Tile t+1 loads into the other stage while tile
 // t is computed.
 //
-// Warp roles (416 threads):
+// Warp roles (384 threads):
 //   warp 0      TMA: Q once per unit and the S operand (completion counted on the even
-//               CTA's barriers, which gate the MMAs)
+//               CTA's barriers, which gate the MMAs); L2 prefetch of the next tile's rows
 //   warp 1      TMEM allocation; TMA of the V operand (local barrier)
 //   warp 2      S MMA issuer (even CTA only)
 //   warp 3      PV MMA issuer (even CTA only)
 //   warps 4-11  softmax (lane r + 64h: query row r over tile half h; warps 4-7 take S
 //               columns 0-31 and O block 0, warps 8-11 columns 32-63 and O block 1),
 //               O rescale, epilogue
-//   warp 12     L2 prefetch of this CTA's upcoming KV rows
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -56,14 +55,13 @@
 namespace mla {
 namespace {
 
-constexpr int kPairThreads = 416;
+constexpr int kPairThreads = 384;
 constexpr uint32_t kPSlab = 8192;  // 64 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffStage = kOffQ + 9 * kPSlab;       // 2 stages x 9 dim slabs of the tile's KV rows
 constexpr uint32_t kStageBytes = 9 * kPSlab;
 constexpr uint32_t kOffP1 = kOffStage + 2 * kStageBytes;  // P of KV rows 64-127 (rows 0-63: the stage's RoPE slab)
 constexpr uint32_t kOffMisc = kOffP1 + kPSlab;
-constexpr uint32_t kPairPrefetchBytes = 72u * 1024u;  // one tile: farther ahead thrashes L2 and slows the loads
 constexpr float kPairRescaleLog2 = 32.0f;
 // A stage arrives in three parts of three dim slabs (slabs 3p .. 3p + 2), each on its own
 // barrier, so that the S MMAs of the first slabs run while the later ones are still landing.
@@ -98,7 +96,7 @@ struct PairMisc {
   uint64_t bar[kNumPairBars];
   uint32_t tmem_base;
   int abort;
-  int progress;  // tiles whose S operand loads have been issued (throttles the L2 prefetch)
+  int pad2;
   int pad;
   // the four threads of a query row exchange their tile maxima (slow path of a tile) and,
   // at the end of a unit, their partial sums here
@@ -142,7 +140,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     mbar_init(bar(kOFull), 1);
     mbar_init(bar(kFinal), 2);
     misc->abort = 0;
-    misc->progress = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -239,7 +236,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                                    lead(kSRegFull + kStageParts * st + s / 3));
                 }
             }
-            *reinterpret_cast<volatile int*>(&misc->progress) = it + 1;
+            // Streams this CTA's rows of the unit's next tile from HBM into L2 (a hint; one bulk
+            // prefetch per page box). Measured on the 128-head bf16 workload: one tile ahead
+            // shortens the S-operand loads by a third; two tiles ahead gains nothing more, and
+            // four or more slow the kernel (L2 thrashing).
+            if (own + 2 < hi) {
+              const int nxt = own + 2;
+              for (int k = 0; k < nbox; ++k) {
+                const int pos0 = nxt * kBlockRows + k * box_rows;
+                if (pos0 >= L) break;
+                const int pi = pos0 >> P.log2_ps;
+                const int page = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
+                if (page < 0 || page >= P.num_pages) continue;
+                const int rows = (L - pos0) < box_rows ? (L - pos0) : box_rows;
+                prefetch_l2_bulk(P.kv + static_cast<int64_t>(page) * P.page_bytes +
+                                     static_cast<int64_t>(pos0 & (P.page_size - 1)) * P.row_bytes,
+                                 static_cast<uint32_t>(rows * P.row_bytes));
+              }
+            }
           }
         });
       }
@@ -557,30 +571,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         if (wait(bar(kOFull), u & 1)) {
           tc_fence_after();
-          const int64_t orow = (nsplit == 1 ? (int64_t)rq : (int64_t)sg) * R + grow;
+          // A warp holds 32 consecutive output rows (one per lane) and, per TMEM load, the same
+          // 32 value dims of each. Eight rows at a time pass through this warp's 1-KiB slice of
+          // the P slab (free here: the unit's last PV has completed; 16-B chunk q of staged row i
+          // at position q ^ i), so that each global store covers contiguous dims of one row
+          // (a store of one 16-B chunk per lane would touch 32 rows).
+          const uint32_t xb = sb + kOffP1 + static_cast<uint32_t>(warp - 4) * 1024u;
+          const int64_t row0 = (nsplit == 1 ? (int64_t)rq : (int64_t)sg) * R + (grow - lane);
 #pragma unroll 1
           for (int k = 0; k < 4; ++k) {
             uint32_t t32[32];
             tmem_ld32(tmem_o + lane_off + cg * 128 + k * 32, t32);
             tmem_wait_ld();
             const int d0 = cg * 256 + half * 128 + k * 32;  // first value dim of these 32 columns
-            if (nsplit == 1) {
-              uint4* o = reinterpret_cast<uint4*>(P.out + orow * 512 + d0);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint32_t w4[4];
+            for (int rnd = 0; rnd < 4; ++rnd) {
+              if ((lane >> 3) == rnd) {
+                const uint32_t i = static_cast<uint32_t>(lane & 7);
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  w4[e] = f32x2_to_bf16x2(__uint_as_float(t32[8 * q + 2 * e]) * inv,
-                                          __uint_as_float(t32[8 * q + 2 * e + 1]) * inv);
-                o[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                for (int q = 0; q < 8; ++q)
+                  st_shared_v4(xb + i * 128 + ((static_cast<uint32_t>(q) ^ i) << 4),
+                               make_uint4(__float_as_uint(__uint_as_float(t32[4 * q]) * inv),
+                                          __float_as_uint(__uint_as_float(t32[4 * q + 1]) * inv),
+                                          __float_as_uint(__uint_as_float(t32[4 * q + 2]) * inv),
+                                          __float_as_uint(__uint_as_float(t32[4 * q + 3]) * inv)));
               }
-            } else {
-              float4* o = reinterpret_cast<float4*>(P.part_out + orow * 512 + d0);
+              __syncwarp();
+              if (nsplit == 1) {
+                // bf16: 16 lanes per row, two dims each, two rows per store
+                const int m = lane & 15;
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                o[q] = make_float4(__uint_as_float(t32[4 * q]) * inv, __uint_as_float(t32[4 * q + 1]) * inv,
-                                   __uint_as_float(t32[4 * q + 2]) * inv, __uint_as_float(t32[4 * q + 3]) * inv);
+                for (int i2 = 0; i2 < 8; i2 += 2) {
+                  const uint32_t i = static_cast<uint32_t>(i2 + (lane >> 4));
+                  const float2 v = ld_shared_v2f32(xb + i * 128 + ((static_cast<uint32_t>(m >> 1) ^ i) << 4) + (m & 1) * 8);
+                  reinterpret_cast<uint32_t*>(P.out + (row0 + rnd * 8 + i) * 512 + d0)[m] = f32x2_to_bf16x2(v.x, v.y);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float v = ld_shared_f32(xb + i * 128 + ((static_cast<uint32_t>(lane >> 2) ^ i) << 4) + (lane & 3) * 4);
+                  P.part_out[(row0 + rnd * 8 + i) * 512 + d0 + lane] = v;
+                }
+              }
+              __syncwarp();
             }
           }
           tc_fence_before();
@@ -588,44 +621,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         __syncwarp();
         if (lane == 0 && !dead) mbar_arrive_cluster(lead(kOFree));
         ++u;
-      });
-    }
-  } else if (warp == 12) {
-    // ------------------------------------------------------------ L2 prefetch
-    // Streams this CTA's KV rows of the next tile (and the next units' Q rows) from HBM into
-    // L2 one tile ahead of the S-operand loads: one bulk prefetch per page block (a copy
-    // instruction costs about the same whatever its size). A hint only. Measured on the
-    // 128-head bf16 workload: one tile ahead shortens the S-operand loads by a third; two
-    // tiles ahead gains nothing more, and four or more slow the kernel (L2 thrashing).
-    int ahead = static_cast<int>(kPairPrefetchBytes / (static_cast<uint32_t>(kBlockRows) * P.row_bytes));
-    ahead = ahead < 1 ? 1 : ahead;
-    int pit = 0;
-    for (int w = cl0; w < num_work && !*abort_flag; w += ncl) {
-      const int part = w / PG, g = w % PG;
-      for_each_unit(P, part, [&](int r, int lo, int hi, int) {
-        if (*abort_flag) return;
-        if (lane == 0)
-          prefetch_l2_bulk(P.q + (static_cast<int64_t>(r) * R + g * 128 + 64 * c) * 576, 64u * 576u * 2u);
-        const int L = request_len(P, r);
-        for (int b0 = lo; b0 < hi; b0 += 2, ++pit) {
-          const uint64_t t0 = globaltimer();
-          while (pit >= *reinterpret_cast<volatile int*>(&misc->progress) + ahead) {
-            if (*abort_flag) return;
-            if (globaltimer() - t0 > 20000000ull) break;  // stop throttling after 20 ms
-            __nanosleep(256);
-          }
-          const int own = b0 + c;
-          if (own >= hi || lane >= nbox) continue;
-          const int pos0 = own * kBlockRows + lane * box_rows;
-          if (pos0 >= L) continue;
-          const int pi = pos0 >> P.log2_ps;
-          const int page = pi < P.max_pages ? P.block_table[static_cast<int64_t>(r) * P.max_pages + pi] : -1;
-          if (page < 0 || page >= P.num_pages) continue;
-          const int rows = (L - pos0) < box_rows ? (L - pos0) : box_rows;
-          prefetch_l2_bulk(P.kv + static_cast<int64_t>(page) * P.page_bytes +
-                               static_cast<int64_t>(pos0 & (P.page_size - 1)) * P.row_bytes,
-                           static_cast<uint32_t>(rows * P.row_bytes));
-        }
       });
     }
   }
