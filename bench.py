@@ -353,6 +353,15 @@ def time_rig(rig, args, flush, stream, dist, dev, local):
             "clocks": clocks, "nbd": nbd}
 
 
+def decode_kernel_name(w):
+    """The decode kernel mla_decode launches for this workload: dense bf16 rows whose query
+    rows per request come in groups of 128 run on CTA pairs, everything else on the
+    single-SM kernel."""
+    c = w.cfg
+    pair = c.layout == 0 and c.topk == 0 and (c.sq * c.heads) % 128 == 0
+    return "mla_decode_pair_kernel" if pair else "mla_decode_kernel"
+
+
 def roofline_of(w, name, dec_ms, peaks, peak_src):
     """The decode kernel against the slower of its algorithmic bytes at the HBM peak and its
     algorithmic FLOPs at the bf16 tensor peak: the measured peaks (MEASURED_PEAKS.json,
@@ -373,7 +382,7 @@ def roofline_of(w, name, dec_ms, peaks, peak_src):
     roof.update({"traffic": recorded_traffic(name),
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
                  "nominal_peak": NOMINAL_PEAKS["hbm_gbs"] if roof["bound"] == "hbm" else NOMINAL_PEAKS["bf16_tflops"],
-                 "kernel": "mla_decode_kernel", "alg_bytes_per_launch": cost["bytes"],
+                 "kernel": decode_kernel_name(w), "alg_bytes_per_launch": cost["bytes"],
                  "alg_flops_per_launch": cost["flops"], "kernel_ms": statistics.mean(dec_ms),
                  "roofline_ms": 1e3 * max(t_hbm, t_tc)})
     return roof, cost
