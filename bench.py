@@ -541,6 +541,69 @@ def next_row_extras(rig, flush, stream, dev, nbd):
     return res
 
 
+def sparse_prefill_entry(flush, stream, dev, nbd, num_sms, peaks, peak_src, cpu_budget_s):
+    """mla_sparse_prefill (flash_mla_sparse_fwd's contract) on a prefill-shaped batch: 512 query
+    tokens x 128 heads over one unpaged bf16 latent run of 32768 rows, 2048 distinct indices
+    per token (seeded), sm_scale 1/sqrt(192); the decode + combine timed with CUDA events,
+    L2 flushed. Bound by the tensor pipe: the gathered rows are reused across tokens."""
+    import torch
+    import mla_paged_latent_gb300 as mla
+    T, N, s_kv, topk = 512, 128, 32768, 2048
+    gen = torch.Generator(device=dev).manual_seed(11)
+    q = torch.randn(T, N, 576, device=dev, generator=gen).to(torch.bfloat16)
+    kv = torch.randn(s_kv, 576, device=dev, generator=gen).to(torch.bfloat16)
+    idx = torch.rand(T, s_kv, device=dev, generator=gen).argsort(dim=1)[:, :topk].to(torch.int32).contiguous()
+    scale = 1.0 / math.sqrt(192.0)
+    plan = mla.mla_decode_plan(np.full(T, s_kv, np.int32), 1, N, topk, 1, num_sms)
+    sched, ns = torch.from_numpy(plan.sched).to(dev), torch.from_numpy(plan.num_splits).to(dev)
+    ws = mla.alloc_workspace(plan.workspace_bytes, dev)
+    out = torch.empty(T, N, 512, dtype=torch.bfloat16, device=dev)
+    mx = torch.empty(T, N, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, N, dtype=torch.float32, device=dev)
+    evs = []
+    for k in range(nbd + 3):
+        flush.fill_(k & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        mla.mla_sparse_prefill(q, kv, idx, scale, sched, ns, plan.num_partitions, plan.total_splits, ws, out, mx, lse,
+                               stream=stream)
+        e1.record(stream)
+        if k >= 3:
+            evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    assert mla.mla_read_status(ws) == 0
+    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    flops = 2.0 * T * N * topk * (576 + 512)
+    nbytes = T * N * 576 * 2 + s_kv * 1152 + T * topk * 4 + T * N * (512 * 2 + 4 + 4)
+    tflops = flops / (us * 1e-6) / 1e12
+    entry = {"config": {"workload": f"sparse prefill: {T} tokens x {N} heads, unpaged bf16 latent run of {s_kv} "
+                                    f"rows, {topk} indices per token, sm_scale 1/sqrt(192)"},
+             "value": T / (us * 1e-6), "unit": UNIT, "kernel_us": us,
+             "plan": {"partitions": plan.num_partitions, "total_splits": plan.total_splits},
+             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                          "frac": tflops / peaks["bf16_tflops"],
+                          "frac_of_nominal": tflops / NOMINAL_PEAKS["bf16_tflops"], "traffic": None,
+                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
+                          "alg_flops_per_launch": flops, "alg_bytes_per_launch": nbytes,
+                          "kernel": "mla_decode_kernel (bf16 gather) + combine_kernel"},
+             "cpu_baseline": None}
+    if cpu_budget_s > 0:
+        import oracle
+        oracle.build()
+        q_bits = q.view(torch.int16).cpu().numpy().view(np.uint16)
+        kv_bits = kv.view(torch.int16).cpu().numpy().view(np.uint16)
+        idx_h = idx.cpu().numpy()
+        t0, done = time.perf_counter(), 0
+        while done == 0 or (time.perf_counter() - t0 < cpu_budget_s and done < T):
+            oracle.sparse_prefill(q_bits[done:done + 4], kv_bits, idx_h[done:done + 4], scale)
+            done += 4
+        dt = time.perf_counter() - t0
+        entry["cpu_baseline"] = {"value": done / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": f"{done} query tokens x {N} heads of the same batch, fp64 C oracle, "
+                                           f"OpenMP over tokens, {dt:.1f} s"}
+    return entry
+
+
 def run_e2e(rig, args, dist, dev, world):
     """End to end through the public API with host buffers (pinned), copies inside the
     timed region. A serving loop: every step plans on the host, copies its inputs host ->
@@ -731,6 +794,10 @@ def main():
             launches += r2.launches_per_step * args.steps
             others[name] = entry
             del r2
+        torch.cuda.empty_cache()
+        others["sparse_prefill"] = sparse_prefill_entry(
+            flush, stream, dev, max(5, min(tm["nbd"], 20)), num_sms, peaks, peak_src,
+            5.0 if (world == 1 and rank == 0 and not args.no_cpu_baseline) else 0.0)
 
     if rank != 0:
         if dist is not None:
