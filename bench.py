@@ -5,7 +5,8 @@ One step = one pass of the whole path over one batch: mla_kv_write of the
 batch's new rows, then mla_decode (persistent decode kernel) and, for requests
 the plan split, mla_combine. Inputs are resident in HBM when the timed region
 starts; L2 is flushed (a 256 MiB buffer is overwritten) between steps, outside
-each step's CUDA-event pair.
+each step's CUDA-event pair, unless a step reads more than twice the L2 size (then
+no flush: inputs larger than L2; the line's config says which).
 
 Default workload (N=1): the DeepSeek-V3-shaped bf16 decode batch — 64 requests
 x 1 token, 128 heads, bf16 latent KV rows [512 | 64], context lengths
@@ -248,11 +249,27 @@ CONFIG_DESC = {
 NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 
 
+L2_BYTES = 129 << 20  # GB300 L2 (the device property is used when torch reports it)
+
+
+def l2_policy(w, l2_bytes=L2_BYTES):
+    """Between timed steps, L2 is flushed (a 256 MiB buffer overwritten) unless the bytes one
+    step must read are more than twice the L2 size: such inputs cannot stay in L2 from one
+    step to the next, and a flush would leave 129 MB of dirty lines whose write-back then
+    competes with the measured step."""
+    nbytes = algorithmic_cost(w)["bytes"]
+    flush = nbytes < 2 * l2_bytes
+    note = ("flushed between steps (256 MiB write)" if flush else
+            f"not flushed: inputs larger than L2 (a step reads {nbytes / 1e6:.0f} MB, more than twice the "
+            f"{l2_bytes / 1e6:.0f} MB L2)")
+    return flush, note
+
+
 def config_dict(w, name):
     c = w.cfg
     return {"workload": CONFIG_DESC[name], "batch": c.batch, "q_tokens_per_req": c.sq, "heads": c.heads,
             "kv_layout": ["bf16-576", "fp8-448-ue8m0", "fp8-512-ue8m0"][c.layout], "page_size": c.page_size,
-            "kv_rows": int(w.seqlens.sum()), "seed": c.seed, "l2": "flushed between steps (256 MiB write)"}
+            "kv_rows": int(w.seqlens.sum()), "seed": c.seed, "l2": l2_policy(w)[1]}
 
 
 class Rig:
@@ -317,11 +334,14 @@ class Rig:
 
 def time_rig(rig, args, flush, stream, dist, dev, local):
     """W warm-up steps, then K timed steps (CUDA events at the step boundaries, L2 flushed
-    between steps outside the event pairs, nvidia-smi clocks sampled meanwhile), then a
-    breakdown pass with events between the kernels."""
+    between steps outside the event pairs unless the inputs are larger than L2 (l2_policy),
+    nvidia-smi clocks sampled meanwhile), then a breakdown pass with events between the
+    kernels."""
     torch, mla = rig.torch, rig.mla
+    do_flush = l2_policy(rig.w)[0]
     for _ in range(args.warmup):
-        flush.fill_(1)
+        if do_flush:
+            flush.fill_(1)
         rig.step(stream)
     torch.cuda.synchronize(dev)
     mla.mla_read_status(rig.ws)
@@ -333,7 +353,8 @@ def time_rig(rig, args, flush, stream, dist, dev, local):
     sampler.start()
     time.sleep(0.15)
     for k in range(args.steps):
-        flush.fill_(k & 0xFF)
+        if do_flush:
+            flush.fill_(k & 0xFF)
         rig.step(stream, events[k])
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
@@ -344,7 +365,8 @@ def time_rig(rig, args, flush, stream, dist, dev, local):
     nbd = min(args.steps, 50)
     bd = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(nbd)]
     for k in range(nbd):
-        flush.fill_(k & 0xFF)
+        if do_flush:
+            flush.fill_(k & 0xFF)
         rig.step(stream, bd[k], breakdown=True)
     torch.cuda.synchronize(dev)
     mla.mla_read_status(rig.ws)
