@@ -452,6 +452,8 @@ SMALL = {
     # the smallest page (8 TMA boxes per 64-row slab), empty requests on the bf16 TMA path,
     # a head count that is not a multiple of 16, and the largest query-row count (32 x 128)
     "dsv3_ps8": lambda: workloads.dsv3(batch=3, seqlens=(5, 64, 333), len_dist="fixed", page_size=8),
+    "dsv3_ps256": lambda: workloads.dsv3(batch=3, seqlens=(300, 513, 1500), len_dist="fixed", page_size=256),
+    "dsv3_sink": lambda: workloads.dsv3(batch=3, seqlens=(100, 700, 1500), len_dist="fixed", sink=True),
     "empty_bf16": lambda: workloads.dsv3(batch=4, seqlens=(0, 65, 0, 3), len_dist="fixed", new_rows=False),
     "heads20": lambda: workloads.dsv3(batch=2, heads=20, seqlens=(100, 700), len_dist="fixed"),
     "rows4096": lambda: workloads.verify(batch=1, sq=32, seqlens=(200,), len_dist="fixed"),
@@ -502,8 +504,8 @@ def test_decode_forced_splits(name, num_sms):
                      bound_for(w.cfg.layout))
 
 
-PAIR_CASES = ["dsv3_small", "verify_small", "dsv3_ps16", "dsv3_ps8", "verify_sq2_h64", "tail_nan_bf16",
-              "empty_bf16", "rows4096"]
+PAIR_CASES = ["dsv3_small", "verify_small", "dsv3_ps16", "dsv3_ps8", "dsv3_ps256", "dsv3_sink", "verify_sq2_h64",
+              "tail_nan_bf16", "empty_bf16", "rows4096"]
 
 
 @pytest.mark.parametrize("name", PAIR_CASES)
@@ -522,7 +524,7 @@ def test_decode_pair_and_single_sm_kernels(name, min_splits):
     for single in (False, True):
         d.out.fill_(float("nan"))
         mla.mla_decode(d.q, d.kv, c.layout, c.page_size, d.bt, d.sl, c.sq, c.sm_scale, d.sched, d.ns,
-                       d.plan.num_partitions, d.plan.total_splits, d.ws, d.out, d.lse, causal=c.causal,
+                       d.plan.num_partitions, d.plan.total_splits, d.ws, d.out, d.lse, sink=d.sink, causal=c.causal,
                        single_sm=single)
         assert mla.mla_read_status(d.ws) == 0
         out = d.out.float().cpu().numpy().astype(np.float64)
@@ -540,11 +542,12 @@ def test_decode_deterministic():
     assert np.array_equal(a, b) and np.array_equal(la, d.lse.cpu().numpy())
 
 
-def test_large_score_growth_triggers_rescale():
+@pytest.mark.parametrize("heads", [64, 128])
+def test_large_score_growth_triggers_rescale(heads):
     """Scores that grow along the sequence force the lazy O rescale (the running
     max rises by more than 2^32 between tiles several times: the RoPE scores grow
-    to ~200 in log2 units)."""
-    cfg = workloads.dsv3(batch=2, heads=64, seqlens=(640, 1000), len_dist="fixed", new_rows=False)
+    to ~200 in log2 units). 64 heads run on the single-SM kernel, 128 on CTA pairs."""
+    cfg = workloads.dsv3(batch=2, heads=heads, seqlens=(640, 1000), len_dist="fixed", new_rows=False)
     w = workloads.generate(cfg)
     # scale the RoPE part of KV rows up with position so that later tiles dominate
     ps = cfg.page_size
@@ -562,7 +565,7 @@ def test_large_score_growth_triggers_rescale():
     d = DeviceWorkload(w)
     out, lse = d.run()
     ref_out, ref_lse = oracle_decode(w)
-    assert_close(out, lse, ref_out, ref_lse, "rescale")
+    assert_close(out, lse, ref_out, ref_lse, f"rescale, {heads} heads")
 
 
 def _scale_rope_with_position(w, row_bytes, nope_bytes, growth):
