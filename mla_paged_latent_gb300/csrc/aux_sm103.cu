@@ -17,7 +17,7 @@ __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_floa
 // ----------------------------------------------------------------------------- combine
 // One warp per query row of a request that the plan split into >= 2 pieces (the merge
 // itself is merge_row in combine_row.cuh).
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_out,
                                                       const float* __restrict__ part_lse,
                                                       const int32_t* __restrict__ num_splits, int R, int heads,
                                                       const float* __restrict__ sink, uint16_t* __restrict__ out,
@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int s0 = num_splits[b];
   const int ns = num_splits[b + 1] - s0;
   if (ns < 2) return;
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   if (row >= R) return;
   const int lane = threadIdx.x & 31;
   const int64_t orow = (int64_t)b * R + row;
@@ -404,8 +404,10 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
                            int rows_per_req, int heads, const float* sink, uint16_t* out, float* lse,
                            const float* part_max, float* max_logits, cudaStream_t stream) {
   if (batch <= 0 || rows_per_req <= 0) return cudaSuccess;
-  dim3 grid((rows_per_req + 7) / 8, batch);
-  return launch_pdl(combine_kernel, grid, dim3(256), 0, stream, part_out, part_lse, num_splits, rows_per_req, heads,
+  // one warp per row, four rows per 128-thread block (96 registers a thread: five blocks
+  // per SM, against two of 256 threads)
+  dim3 grid((rows_per_req + 3) / 4, batch);
+  return launch_pdl(combine_kernel, grid, dim3(128), 0, stream, part_out, part_lse, num_splits, rows_per_req, heads,
                     sink, out, lse, part_max, max_logits);
 }
 
