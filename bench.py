@@ -159,15 +159,22 @@ def _code_tokens(text):
     return " ".join("".join(out).split())
 
 
+# The sources that make the decode kernels and their launches (tensor maps, grid, plan):
+# the recorded ncu counters of a decode launch depend on these and on nothing else.
+DECODE_SOURCES = ("mla_paged_latent_gb300/csrc/api.cpp", "mla_paged_latent_gb300/csrc/plan.cpp",
+                  "mla_paged_latent_gb300/csrc/decode_sm103.cu", "mla_paged_latent_gb300/csrc/decode_pair_sm103.cu",
+                  "mla_paged_latent_gb300/csrc/decode_common.cuh", "mla_paged_latent_gb300/csrc/ptx_sm103.cuh",
+                  "mla_paged_latent_gb300/csrc/mla_kernels.h", "include/mla_decode.h")
+
+
 def source_hash():
-    """Hash of the library's code (csrc, comments and layout of whitespace aside): the
-    recorded ncu counters stay valid while it is unchanged."""
+    """Hash of the decode kernels' code (DECODE_SOURCES; comments and layout of whitespace
+    aside): the recorded ncu counters of the decode stay valid while it is unchanged."""
     import hashlib
     h = hashlib.sha256()
-    d = os.path.join(ROOT, "mla_paged_latent_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        with open(os.path.join(d, name), encoding="utf-8") as f:
-            h.update(name.encode() + _code_tokens(f.read()).encode())
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(rel.encode() + _code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 

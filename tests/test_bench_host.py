@@ -12,17 +12,26 @@ def test_code_tokens_drop_comments_keep_literals():
 
 
 def test_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
-    src = os.path.join(bench.ROOT, "mla_paged_latent_gb300", "csrc")
-    dst = tmp_path / "mla_paged_latent_gb300" / "csrc"
-    shutil.copytree(src, dst)
+    for sub in ("mla_paged_latent_gb300/csrc", "include"):
+        shutil.copytree(os.path.join(bench.ROOT, sub), tmp_path / sub)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.source_hash()
-    p = dst / "combine_row.cuh"
+    # a comment and blank lines in a decode source: same hash
+    p = tmp_path / "mla_paged_latent_gb300" / "csrc" / "decode_common.cuh"
     text = p.read_text()
     p.write_text("// an added comment line\n" + text.replace("\n", "\n\n", 3))
     assert bench.source_hash() == h0
-    p.write_text(text.replace("acc[i] *= f;", "acc[i] *= 2.f * f;", 1))
+    # code of a decode source: a new hash
+    assert "ex2.approx.ftz.f32" in text
+    p.write_text(text.replace("ex2.approx.ftz.f32", "ex2.approx.f32", 1))
     assert bench.source_hash() != h0
+    p.write_text(text)
+    # code outside the decode kernels (the combine's merge): the decode's counters stay valid
+    q = tmp_path / "mla_paged_latent_gb300" / "csrc" / "combine_row.cuh"
+    qt = q.read_text()
+    assert "acc[i] *= f;" in qt
+    q.write_text(qt.replace("acc[i] *= f;", "acc[i] *= 2.f * f;", 1))
+    assert bench.source_hash() == h0
 
 
 def test_algorithmic_cost_tiny_closed_form():
