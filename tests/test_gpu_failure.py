@@ -28,18 +28,19 @@ def _lib():
     mla.load()
 
 
-@pytest.mark.parametrize("cfg", [
-    lambda: workloads.dsv3(batch=3, seqlens=(64, 700, 1300), len_dist="fixed", new_rows=False),
-    lambda: workloads.dsv4(batch=3, seqlens=(64, 700, 1300), len_dist="fixed", new_rows=False),
-], ids=["bf16_tma", "fp8_converters"])
-def test_wait_timeout_is_reported_and_context_survives(cfg):
+@pytest.mark.parametrize("cfg,single_sm", [
+    (lambda: workloads.dsv3(batch=3, seqlens=(64, 700, 1300), len_dist="fixed", new_rows=False), False),
+    (lambda: workloads.dsv3(batch=3, seqlens=(64, 700, 1300), len_dist="fixed", new_rows=False), True),
+    (lambda: workloads.dsv4(batch=3, seqlens=(64, 700, 1300), len_dist="fixed", new_rows=False), False),
+], ids=["bf16_cta_pair", "bf16_tma_single_sm", "fp8_converters"])
+def test_wait_timeout_is_reported_and_context_survives(cfg, single_sm):
     w = workloads.generate(cfg())
     c = w.cfg
     d = DeviceWorkload(w)
     p = d.make_plan()
     t0 = time.monotonic()
     mla.mla_decode(d.q, d.kv, c.layout, c.page_size, d.bt, d.sl, c.sq, c.sm_scale, d.sched, d.ns, p.num_partitions,
-                   p.total_splits, d.ws, d.out, d.lse, sink=d.sink, _test_withhold_signal=True)
+                   p.total_splits, d.ws, d.out, d.lse, sink=d.sink, single_sm=single_sm, _test_withhold_signal=True)
     torch.cuda.synchronize()
     elapsed = time.monotonic() - t0
     status = int(d.ws[:4].cpu().numpy().view(np.uint32)[0])
