@@ -19,10 +19,11 @@
 //               16 MMAs per tile for the 512 dims. CTA c's accumulator holds O of its
 //               own 64 rows for all 512 dims: lane r + 64h, column 128b + d is dim
 //               256b + 128h + d. Rescales and the epilogue therefore stay inside a CTA.
-// Each full-rate pair instruction moves both SMs: these two shapes run at the
-// tensor cores' full rate per SM (64 cycles per K = 16 step), where the single-SM
-// shapes of decode_sm103.cu (M = 128 with 64 rows used, N = 64) run at a quarter to
-// two thirds of it.
+// Measured on GB300 with distinct operands and fully unrolled issue: the PV shape runs
+// at the tensor cores' full rate per SM (64 cycles per K = 16 step), the S shape in 49
+// cycles (about two thirds of it: the smallest pair instruction is bound by its issue);
+// for the same query rows and KV rows the single-SM kernel needs twice the S instructions
+// (M = 128 with 64 rows used, N = 64).
 //
 // Shared memory per CTA (224 KiB): Q (9 slabs of 64 rows x 64 dims, 128-B swizzle) and
 // two stages of 9 dim slabs for the tile's KV rows, plus one 8-KiB P slab. A tile's stage
