@@ -159,35 +159,37 @@ def _code_tokens(text):
     return " ".join("".join(out).split())
 
 
-# The sources that make the decode kernels and their launches (tensor maps, grid, plan):
-# the recorded ncu counters of a decode launch depend on these and on nothing else.
-DECODE_SOURCES = ("mla_paged_latent_gb300/csrc/api.cpp", "mla_paged_latent_gb300/csrc/plan.cpp",
-                  "mla_paged_latent_gb300/csrc/decode_sm103.cu", "mla_paged_latent_gb300/csrc/decode_pair_sm103.cu",
-                  "mla_paged_latent_gb300/csrc/decode_common.cuh", "mla_paged_latent_gb300/csrc/ptx_sm103.cuh",
-                  "mla_paged_latent_gb300/csrc/mla_kernels.h", "include/mla_decode.h")
+# The sources that make each decode kernel and its launches (tensor maps, grid, plan): the
+# recorded ncu counters of a decode launch depend on these and on nothing else.
+DECODE_COMMON = ("mla_paged_latent_gb300/csrc/api.cpp", "mla_paged_latent_gb300/csrc/plan.cpp",
+                 "mla_paged_latent_gb300/csrc/decode_common.cuh", "mla_paged_latent_gb300/csrc/ptx_sm103.cuh",
+                 "mla_paged_latent_gb300/csrc/mla_kernels.h", "include/mla_decode.h")
+DECODE_SOURCES = {"mla_decode_pair_kernel": DECODE_COMMON + ("mla_paged_latent_gb300/csrc/decode_pair_sm103.cu",),
+                  "mla_decode_kernel": DECODE_COMMON + ("mla_paged_latent_gb300/csrc/decode_sm103.cu",)}
 
 
-def source_hash():
-    """Hash of the decode kernels' code (DECODE_SOURCES; comments and layout of whitespace
-    aside): the recorded ncu counters of the decode stay valid while it is unchanged."""
+def source_hash(kernel="mla_decode_pair_kernel"):
+    """Hash of one decode kernel's code (DECODE_SOURCES[kernel]; comments and layout of
+    whitespace aside): the recorded ncu counters of that kernel stay valid while it is
+    unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for rel in DECODE_SOURCES:
+    for rel in DECODE_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             h.update(rel.encode() + _code_tokens(f.read()).encode())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config_name):
+def recorded_traffic(config_name, kernel):
     """Per-launch DRAM bytes of the decode kernel from a committed ncu summary,
-    valid only while the kernel sources are unchanged."""
+    valid only while that kernel's sources are unchanged."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
         e = d.get(config_name)
-        if e and e.get("source_hash") == source_hash():
+        if e and e.get("kernel") == kernel and e.get("source_hash") == source_hash(kernel):
             return e.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -408,7 +410,7 @@ def roofline_of(w, name, dec_ms, peaks, peak_src):
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"],
                 "frac_of_nominal": achieved / NOMINAL_PEAKS["bf16_tflops"]}
-    roof.update({"traffic": recorded_traffic(name),
+    roof.update({"traffic": recorded_traffic(name, decode_kernel_name(w)),
                  "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback",
                  "nominal_peak": NOMINAL_PEAKS["hbm_gbs"] if roof["bound"] == "hbm" else NOMINAL_PEAKS["bf16_tflops"],
                  "kernel": decode_kernel_name(w), "alg_bytes_per_launch": cost["bytes"],

@@ -383,7 +383,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (globaltimer() - t0 > 20000000ull) break;  // stop throttling after 20 ms
             __nanosleep(256);
           }
-          if (sparse) {
+          if (sparse && LAYOUT != 0 && !runs) {
+            // fp8 rows gathered by top-k index get no L2 hints: measured on the sparse top-k
+            // workload (fp8-512), per-row hints three tiles ahead raised DRAM traffic from 1.12x
+            // to 1.35x the algorithmic bytes (rows evicted before their gather) and made the
+            // kernel 2 % slower. bf16 gathers (sparse prefill: rows shared by many tokens) and
+            // window runs keep them (without: 24 % and 3 % slower).
+          } else if (sparse) {
             // two rows per lane: both indices, then both pages, then the prefetches
             int pos[2], page[2];
 #pragma unroll

@@ -15,23 +15,33 @@ def test_source_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     for sub in ("mla_paged_latent_gb300/csrc", "include"):
         shutil.copytree(os.path.join(bench.ROOT, sub), tmp_path / sub)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    h0 = bench.source_hash()
+    h0 = bench.source_hash("mla_decode_kernel")
+    hp = bench.source_hash("mla_decode_pair_kernel")
     # a comment and blank lines in a decode source: same hash
     p = tmp_path / "mla_paged_latent_gb300" / "csrc" / "decode_common.cuh"
     text = p.read_text()
     p.write_text("// an added comment line\n" + text.replace("\n", "\n\n", 3))
-    assert bench.source_hash() == h0
-    # code of a decode source: a new hash
+    assert bench.source_hash("mla_decode_kernel") == h0
+    # code of a source both decode kernels use: new hashes for both
     assert "ex2.approx.ftz.f32" in text
     p.write_text(text.replace("ex2.approx.ftz.f32", "ex2.approx.f32", 1))
-    assert bench.source_hash() != h0
+    assert bench.source_hash("mla_decode_kernel") != h0
+    assert bench.source_hash("mla_decode_pair_kernel") != hp
     p.write_text(text)
+    # code of the single-SM kernel alone: the pair kernel's counters stay valid
+    sk = tmp_path / "mla_paged_latent_gb300" / "csrc" / "decode_sm103.cu"
+    st = sk.read_text()
+    sk.write_text(st + "\nstatic int unused_probe_value = 1;\n")
+    assert bench.source_hash("mla_decode_kernel") != h0
+    assert bench.source_hash("mla_decode_pair_kernel") == hp
+    sk.write_text(st)
     # code outside the decode kernels (the combine's merge): the decode's counters stay valid
     q = tmp_path / "mla_paged_latent_gb300" / "csrc" / "combine_row.cuh"
     qt = q.read_text()
     assert "acc[i] *= f;" in qt
     q.write_text(qt.replace("acc[i] *= f;", "acc[i] *= 2.f * f;", 1))
-    assert bench.source_hash() == h0
+    assert bench.source_hash("mla_decode_kernel") == h0
+    assert bench.source_hash("mla_decode_pair_kernel") == hp
 
 
 def test_algorithmic_cost_tiny_closed_form():
