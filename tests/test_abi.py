@@ -192,3 +192,27 @@ def test_next_row_entry_points_validation(lib):
                                1 << 20, fake, fake, 0, None) == -1
     assert lib.mla_decode_runs(fake, fake, 1, 4, 64, fake, 128, 2, 2, 16, 0.1, None, fake, fake, 1, 2, fake,
                                1 << 20, fake, fake, 0, None) == -2          # several tokens need heads % 64 == 0
+
+
+def test_sparse_prefill_rejects_bad_arguments(lib):
+    """mla_sparse_prefill validates its arguments on the host before any CUDA call
+    (returns MLA_ERR_INVALID_ARG = -1): missing index list or max_logits, the
+    SKIP_COMBINE flag (its split maxima need the combine), empty sizes, misaligned
+    max_logits."""
+    fake = ctypes.c_void_p(0x100000)
+
+    def rc(**kw):
+        a = dict(q=fake, kv=fake, s_kv=100, idx=fake, topk=16, T=2, N=16, scale=0.1, sched=fake, ns=fake, parts=1,
+                 splits=2, ws=fake, wsb=1 << 20, out=fake, mx=fake, lse=fake, flags=0)
+        a.update(kw)
+        return lib.mla_sparse_prefill(a["q"], a["kv"], a["s_kv"], a["idx"], a["topk"], a["T"], a["N"], a["scale"],
+                                      a["sched"], a["ns"], a["parts"], a["splits"], a["ws"], a["wsb"], a["out"],
+                                      a["mx"], a["lse"], a["flags"], None)
+
+    assert rc(idx=None) == -1
+    assert rc(mx=None) == -1
+    assert rc(flags=1) == -1 and b"SKIP_COMBINE" in lib.mla_last_error()
+    assert rc(s_kv=0) == -1
+    assert rc(topk=0) == -1
+    assert rc(T=0) == -1
+    assert rc(mx=ctypes.c_void_p(0x100002)) == -1
