@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       for (int k = 0; k < 5; ++k) mbar_init(bar(kv_empty(s, k)), 1);
       mbar_init(bar(kSFull + s), 1);
-      mbar_init(bar(kSFree + s), 64);
+      mbar_init(bar(kSFree + s), 128);
       mbar_init(bar(kPFull + s), 128);
     }
     mbar_init(bar(kPvDone), 1);
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // tensor pipe interleaves S(j+1) with PV(j) as soon as P(j) exists, which
     // frees each stage (and starts its refill) as early as possible.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, 0, 0);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(64, 64, 0, 0);  // M = 64: rows over all four lane quarters
       const uint64_t kmaj = sdesc_sw128(0, 16, 1024);  // K-major: Q, K tile
       const uint64_t qa = kmaj | (sb >> 4);
       int it = 0, u = 0;
@@ -447,10 +447,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // a thread whose bounded wait fails only marks itself `dead` and carries on
     // through the barriers, every barrier ORs the mark in, and all four warps stop
     // together at the barrier where it becomes visible.
-    const int wt = tid - 128;                 // 0..127, TMEM lane of this thread
+    const int wt = tid - 128;                 // 0..127, TMEM lane of this thread (O^T: value dims)
     const uint32_t lane_off = static_cast<uint32_t>((wt & ~31)) << 16;
-    const bool row_thread = wt < 64;
-    const int row = wt;
+    // S is an M = 64 accumulator: query row r at TMEM lane 32 (r / 16) + r % 16, so every warp
+    // holds 16 rows, and the threads l and l + 16 of a warp take columns 0-31 and 32-63 of row
+    // 16 w + l (they meet through shuffles)
+    const int row = 16 * (wt >> 5) + (wt & 15);
+    const int half = (wt >> 4) & 1;
     bool dead = false, stop = false;
     auto wait = [&](uint32_t b, uint32_t parity) {
       if (!dead && !mbar_wait(b, parity, abort_flag, P.status)) dead = true;
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (stop) return;
         const int L = runs ? 0x7fffffff : request_len(P, r);
         const int grow = g * kGroupRows + row;          // query row within the request
-        const bool valid_row = row_thread && row < rows_g;
+        const bool valid_row = row < rows_g;
         const int tok = grow / P.heads;
         int lim = L;
         if (P.causal && !sparse) {
@@ -482,19 +485,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const int j = lo + jj;
           const bool first = jj == 0;
           bool need = false;
-          if (row_thread) {
+          {
             const uint32_t par = (itj >> 1) & 1;
             wait(bar(kSFull + st), par);
             if (!TMA_KV) wait(bar(kv_full(st, 0)), par);
           }
-          if (row_thread && !dead) {
+          // (a warp's two half-row threads exchange values below: a dead thread keeps going
+          // through the shuffles with masked data and is stopped at the next barrier)
+          {
             tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld32(tmem_s + st * 64 + lane_off, sr);
-            tmem_ld32(tmem_s + st * 64 + lane_off + 32, sr + 32);
-            tmem_wait_ld();
+            uint32_t sr[32];
+            if (!dead) {
+              tmem_ld16x2_32(tmem_s + st * 64 + lane_off, sr);
+              tmem_wait_ld();
+            }
             tc_fence_before();
-            mbar_arrive(bar(kSFree + st));
+            if (!dead) mbar_arrive(bar(kSFree + st));
             // mask (raw scores; the positive scale is folded into the exponent below)
             uint64_t vmask;
             if (sparse || !TMA_KV) {
@@ -507,25 +513,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               nv = nv < 0 ? 0 : (nv > 64 ? 64 : nv);
               vmask = nv == 64 ? ~0ull : ((1ull << nv) - 1ull);
             }
-            if (!valid_row) vmask = 0;
-            float x[64];
+            if (!valid_row || dead) vmask = 0;
+            const uint32_t hmask = static_cast<uint32_t>(vmask >> (32 * half));
+            float x[32];
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-              x[c] = ((vmask >> c) & 1ull) ? __uint_as_float(sr[c]) : -INFINITY;
+            for (int c = 0; c < 32; ++c) {
+              x[c] = ((hmask >> c) & 1u) ? __uint_as_float(sr[c]) : -INFINITY;
               m4[c & 3] = fmaxf(m4[c & 3], x[c]);
             }
-            const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
+            float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));  // the row's maximum
             m_true = fmaxf(m_true, mt);
             const float m_new = (mt > m_run + kRescaleLog2) ? mt : m_run;
             need = (m_new != m_run) && (m_run != -INFINITY) && !first;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = fast_exp2(m_run - m_use);
             float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[32];
-            uint32_t pl[C::kPSplit ? 32 : 1];
+            uint32_t pk[16];
+            uint32_t pl[C::kPSplit ? 16 : 1];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
+            for (int c = 0; c < 16; ++c) {
               const float p0 = fast_exp2(fmaf(x[2 * c], P.scale_log2, -m_use));
               const float p1 = fast_exp2(fmaf(x[2 * c + 1], P.scale_log2, -m_use));
               ps4[c & 3] += p0 + p1;
@@ -535,22 +543,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                 pl[c] = f32x2_to_bf16x2(p0 - h0, p1 - h1);
               }
             }
-            l_run = l_run * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+            l_run = l_run * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));  // this half's share
             m_run = m_new;
-            misc->alpha[st][row] = need ? alpha : 1.0f;
-            // P^T row `row`: 64 bf16 along KV, K-major 128-B swizzled
+            if (half == 0) misc->alpha[st][row] = need ? alpha : 1.0f;
+            // P^T row `row`: 64 bf16 along KV, K-major 128-B swizzled; this thread's 16-B chunks
+            // are 4 half .. 4 half + 3
             const uint32_t pa = C::parea(sb, st) + row * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-              st_shared_v4(pa + ((c8 ^ (row & 7)) << 4),
-                           make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]));
+            for (int q4 = 0; q4 < 4; ++q4)
+              st_shared_v4(pa + (((4 * half + q4) ^ (row & 7)) << 4),
+                           make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]));
             // the shared P_lo buffer is free once the previous tile's PV has completed
             if (C::kPSplit && (itj == 0 || wait(bar(kPvDone), (itj - 1) & 1))) {
               const uint32_t pla = sb + C::kOffPLo + row * 128;
 #pragma unroll
-              for (int c8 = 0; c8 < 8; ++c8)
-                st_shared_v4(pla + ((c8 ^ (row & 7)) << 4),
-                             make_uint4(pl[4 * c8], pl[4 * c8 + 1], pl[4 * c8 + 2], pl[4 * c8 + 3]));
+              for (int q4 = 0; q4 < 4; ++q4)
+                st_shared_v4(pla + (((4 * half + q4) ^ (row & 7)) << 4),
+                             make_uint4(pl[4 * q4], pl[4 * q4 + 1], pl[4 * q4 + 2], pl[4 * q4 + 3]));
             }
           }
           if (TMA_KV && !sparse) {
@@ -603,7 +612,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const int base_split = P.num_splits[r];
         const int nsplit = P.num_splits[r + 1] - base_split;
         const int sg = base_split + sidx;
-        if (row_thread) {
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);  // the row's sum over both halves
+        if (half == 0) {
           float inv = 0.f, lse2 = -INFINITY;
           if (l_run > 0.f) {
             float denom = l_run;
