@@ -92,11 +92,14 @@ struct Cfg {
   static constexpr bool kPInStage = (kNslab == 9);
   static constexpr uint32_t kOffP = kQBytes + 2 * kStageBytes;
   // fp8 rows carry group scales up to 2^k, so P is passed to the PV MMA as a bf16
-  // pair P = P_hi + P_lo (P_lo = bf16(P - P_hi)): one extra 8 KB buffer, shared by
-  // both stages (its writer waits for the previous PV to finish).
+  // pair P = P_hi + P_lo (P_lo = bf16(P - P_hi)) in extra 8 KB buffers: one per stage
+  // where shared memory allows (8-slab rows), else one shared by both stages, whose
+  // writer then waits for the previous tile's PV to finish.
   static constexpr bool kPSplit = (LAYOUT != 0);
   static constexpr uint32_t kOffPLo = kOffP + (kPInStage ? 0 : 2 * kSlab);
-  static constexpr uint32_t kOffMisc = kOffPLo + (kPSplit ? kSlab : 0);
+  static constexpr int kPLoBufs =
+      !kPSplit ? 0 : (kOffPLo + 2 * kSlab + sizeof(Misc) + 1024 <= 232448 ? 2 : 1);
+  static constexpr uint32_t kOffMisc = kOffPLo + kPLoBufs * kSlab;
   static constexpr uint32_t kSmem = kOffMisc + sizeof(Misc) + 1024;
   static_assert(kSmem <= 232448, "shared memory budget of one CTA");
   static constexpr int kChunks = (LAYOUT == 0) ? 72 : (kNope / 16 + 8);  // 16-B chunks per stored row
@@ -105,6 +108,7 @@ struct Cfg {
   __device__ static uint32_t parea(uint32_t base, int st) {
     return kPInStage ? stage(base, st) + 8 * kSlab : base + kOffP + st * kSlab;
   }
+  __device__ static uint32_t plo(uint32_t base, int st) { return base + kOffPLo + (kPLoBufs == 2 ? st : 0) * kSlab; }
 };
 
 template <int LAYOUT, bool TMA_KV>
@@ -307,7 +311,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (lane == 0) {
       const uint64_t kmaj = sdesc_sw128(0, 16, 1024);     // K-major: P^T
       const uint64_t vmaj = sdesc_sw128(0, kSlab, 1024);  // MN-major: V^T (slab pairs)
-      const uint64_t plo = kmaj | ((sb + C::kOffPLo) >> 4);
       int it = 0, u = 0;
       for (int w = blockIdx.x; w < P.num_work && !*abort_flag; w += gridDim.x) {
         const int part = w / G, g = w % G;
@@ -325,6 +328,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (jj == 0 && u > 0 && !mbar_wait(bar(kOFree), (u - 1) & 1, abort_flag, P.status)) return;
             tc_fence_after();
             const uint64_t pb = kmaj | (C::parea(sb, st) >> 4);
+            const uint64_t plo = kmaj | (C::plo(sb, st) >> 4);
             // compact (rolled) issue loop: the issuing thread must not stall on instruction fetch
             uint64_t vblk = vmaj | (C::stage(sb, st) >> 4);
 #pragma unroll 1
@@ -553,9 +557,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             for (int q4 = 0; q4 < 4; ++q4)
               st_shared_v4(pa + (((4 * half + q4) ^ (row & 7)) << 4),
                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]));
-            // the shared P_lo buffer is free once the previous tile's PV has completed
-            if (C::kPSplit && (itj == 0 || wait(bar(kPvDone), (itj - 1) & 1))) {
-              const uint32_t pla = sb + C::kOffPLo + row * 128;
+            // a P_lo buffer of its own per stage is free as P_hi's is (the stage's tile two back
+            // has completed its PV before this tile's rows were stored); a shared one once the
+            // previous tile's PV has completed
+            if (C::kPSplit && (C::kPLoBufs == 2 || itj == 0 || wait(bar(kPvDone), (itj - 1) & 1))) {
+              const uint32_t pla = C::plo(sb, st) + row * 128;
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4)
                 st_shared_v4(pla + (((4 * half + q4) ^ (row & 7)) << 4),
