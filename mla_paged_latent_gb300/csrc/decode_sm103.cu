@@ -12,7 +12,7 @@
 // One persistent CTA per SM processes work items (partition p, query group g):
 // 64 query rows of one request against the KV blocks of the partition's
 // segments. Per 64-row KV tile:
-//   S   = Q K^T      tcgen05 MMA, M = 128 (query rows; rows >= 64 unused),
+//   S   = Q K^T      tcgen05 MMA, M = 64 query rows (16 in each TMEM lane quarter),
 //                    N = 64 KV rows, K = 576 / 512, fp32 accumulator in TMEM
 //   P   = online softmax of S (exp2 domain, lazy rescale when the running max
 //                    grows by more than kRescaleLog2), written as bf16 to shared memory
@@ -27,7 +27,7 @@
 //   warp 1      TMEM allocator; L2 prefetch of upcoming tiles [layout 2 and bf16 gather: PV issuer]
 //   warp 2      S MMA issuer (one thread)
 //   warp 3      PV MMA issuer (one thread) [layout 2 and bf16 gather: L2 prefetch]
-//   warps 4-7   softmax (warps 4,5: one query row per thread) + O rescale + epilogue
+//   warps 4-7   softmax (16 query rows per warp, two threads per row) + O rescale + epilogue
 //   warps 8-15  converters: fp8 -> bf16 dequantisation and sparse row gathers
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -117,11 +117,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                       const __grid_constant__ CUtensorMap kv_map) {
   using C = Cfg<LAYOUT, TMA_KV>;
   constexpr int NS = C::kNslab;
-  // Warp w runs on SM sub-partition w % 4, and the softmax row threads must be warps 4 and 5
-  // (TMEM lanes 0-63 are open only to warps with w % 4 = 0, 1). The PV issuer runs on warp 3,
-  // away from softmax warp 5, and the L2 prefetch warp takes warp 1 (measured: DSV4-shaped
-  // decode 3 % faster, DSV3-shaped 0.5 %, verify 1.3 %). The sparse variants keep the PV
-  // issuer on warp 1: their prefetch warp does per-row work and they were 3 % slower.
+  // Warp w runs on SM sub-partition w % 4 and reaches TMEM lanes 32 (w % 4) .. + 31, so
+  // the four softmax warps 4-7 cover the four lane quarters of S and O^T. The PV issuer runs
+  // on warp 3 and the L2 prefetch warp takes warp 1 (measured with the softmax on warps 4
+  // and 5: DSV4-shaped decode 3 % faster, DSV3-shaped 0.5 %, verify 1.3 %). The sparse
+  // variants keep the PV issuer on warp 1: their prefetch warp does per-row work and they
+  // were 3 % slower.
   constexpr int kPvWarp = (LAYOUT == 1 || TMA_KV) ? 3 : 1;
   constexpr int kPrefetchWarp = (LAYOUT == 1 || TMA_KV) ? 1 : 3;
   extern __shared__ uint8_t smem_raw[];
@@ -254,8 +255,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ S issuer
-    // (on SMSP 2, away from the softmax warps 4 and 5, whose large unrolled code
-    // would otherwise evict the issue loop from the per-SMSP instruction cache).
+    // (a compact rolled loop: it shares SMSP 2 with softmax warp 6 and converter warps,
+    // whose large unrolled code would otherwise evict it from the instruction cache).
     // S and PV are issued by two threads: a thread that polls a barrier stalls
     // until the MMAs it has queued are dispatched, so a single issuer either
     // leaves the tensor pipe idle while it checks whether P is ready or issues
