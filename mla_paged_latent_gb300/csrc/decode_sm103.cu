@@ -63,10 +63,12 @@ __device__ __forceinline__ int kv_empty(int st, int k) { return kKvEmpty + st * 
 constexpr uint32_t kPrefetchBytes = 160u * 1024u;  // 96-224 KB measured alike; 640 KB 4 % slower (DSV3)
 // Lazy rescale: P = 2^(s - m) is taken against the running maximum m, which is
 // raised (and O^T rescaled in TMEM) only when a tile's maximum exceeds it by
-// more than this many powers of two. P then stays below 2^32, far inside bf16
-// and fp32 range (O^T <= rows x 2^32 x max|V|); a small threshold rescales on
-// most tiles when the scores spread widely (fp8 rows with group scales).
-constexpr float kRescaleLog2 = 32.0f;
+// more than this many powers of two. P then stays below 2^64 (bf16 and fp32 reach
+// 2^128), the running sum below rows x 2^64, and O^T below rows x 2^64 x max|V|,
+// inside fp32 while rows x max|V| < 2^64 (e.g. 2^20 rows of values up to 2^43). A
+// smaller threshold rescales often when the scores spread widely (fp8 rows whose
+// group scales make a few rows score far above the rest).
+constexpr float kRescaleLog2 = 64.0f;
 
 struct Misc {
   uint64_t bar[kNumBars];

@@ -544,9 +544,10 @@ def test_decode_deterministic():
 
 @pytest.mark.parametrize("heads", [64, 128])
 def test_large_score_growth_triggers_rescale(heads):
-    """Scores that grow along the sequence force the lazy O rescale (the running
-    max rises by more than 2^32 between tiles several times: the RoPE scores grow
-    to ~200 in log2 units). 64 heads run on the single-SM kernel, 128 on CTA pairs."""
+    """Scores that grow along the sequence force the lazy O rescale: the RoPE scores grow
+    to ~200 in log2 units, so every query row's running max rises past the threshold
+    (2^64 on the single-SM kernel: 2 to 5 times per row; 2^32 on CTA pairs) between
+    tiles. 64 heads run on the single-SM kernel, 128 on CTA pairs."""
     cfg = workloads.dsv3(batch=2, heads=heads, seqlens=(640, 1000), len_dist="fixed", new_rows=False)
     w = workloads.generate(cfg)
     # scale the RoPE part of KV rows up with position so that later tiles dominate
@@ -586,8 +587,8 @@ def _scale_rope_with_position(w, row_bytes, nope_bytes, growth):
 def test_fp8_score_growth_triggers_rescale(layout):
     """fp8 layouts: scores that grow along the sequence (RoPE part of row j scaled by
     1 + j/8, q's RoPE part 2; ~120 in log2 units at the end) raise the running max
-    past the 2^32 lazy-rescale threshold several times per query row, so O is
-    rescaled in TMEM between tiles. In the 448 layout V includes the RoPE part
+    past the 2^64 lazy-rescale threshold 1 to 4 times per query row (counted on the
+    CPU from the same scores), so O is rescaled in TMEM between tiles. In the 448 layout V includes the RoPE part
     (|V| up to ~450), which the bf16 pair P_hi + P_lo carries within the bound."""
     cfg = workloads.dsv4(batch=2, heads=64, seqlens=(640, 1000), len_dist="fixed", new_rows=False, sink=False,
                          layout=layout)
