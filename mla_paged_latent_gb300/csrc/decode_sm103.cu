@@ -391,11 +391,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             __nanosleep(256);
           }
           if (sparse && LAYOUT != 0 && !runs) {
-            // fp8 rows gathered by top-k index get no L2 hints: measured on the sparse top-k
-            // workload (fp8-512), per-row hints three tiles ahead raised DRAM traffic from 1.12x
-            // to 1.35x the algorithmic bytes (rows evicted before their gather) and made the
-            // kernel 2 % slower. bf16 gathers (sparse prefill: rows shared by many tokens) and
-            // window runs keep them (without: 24 % and 3 % slower).
+            // fp8 rows gathered by top-k index get no L2 hints here (the converters hint each
+            // row one tile ahead): measured on the sparse top-k workload (fp8-512), per-row hints
+            // three tiles ahead raised DRAM traffic from 1.12x to 1.35x the algorithmic bytes
+            // (rows evicted before their gather) and made the kernel 2 % slower. bf16 gathers
+            // (sparse prefill: rows shared by many tokens) and window runs keep them (without:
+            // 24 % and 3 % slower).
           } else if (sparse) {
             // two rows per lane: both indices, then both pages, then the prefetches
             int pos[2], page[2];
@@ -749,6 +750,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           pos_a = pos_b;
           page_a = row_page(pos_b);
           pos_b = row_pos(j + 2);
+          if (sparse && LAYOUT != 0 && !runs && page_a >= 0) {
+            // L2 hints for this thread's share of its row of the next tile: one tile ahead, the
+            // distance at which the hinted rows are still in L2 when gathered (the prefetch warp
+            // gives these rows none; measured on the sparse top-k workload: 2 % faster)
+            const int offn = pos_a & (P.page_size - 1);
+            const uint8_t* pgn = P.kv + (int64_t)page_a * P.page_bytes;
+            const uint8_t* rn = pgn + (int64_t)offn * P.row_bytes;
+            for (int l = part4; l * 128 < P.row_bytes; l += 4) prefetch_l2_line(rn + l * 128);
+            if (part4 == 3) prefetch_l2_line(pgn + (int64_t)P.page_size * P.row_bytes + offn * 8);
+          }
           bool valid = page >= 0;
           if (page == -2 && part4 == 0) atomicOr(P.status, 2u);
           const uint8_t* rowp = nullptr;
