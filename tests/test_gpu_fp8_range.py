@@ -107,11 +107,16 @@ def test_decode_all_codes_wide_scales(layout, mode):
     if mode == "nope_scores":
         assert_close(got_out, got_lse, ref_out, ref_lse, f"layout {layout} {mode}", "scaled")
         return
-    # Values up to 448 * 2^27 of both signs: an output element is a weighted mean whose
-    # terms are up to ~10^6 times larger than the mean itself, so the error of any fp32
-    # accumulation scales with the mean of |V| under the same weights, not with |out|.
-    # That mean is the oracle's decode of the same cache with the NoPE sign bits cleared
-    # (q_nope = 0: the weights depend on the RoPE part only).
+    _assert_within_mean_abs_v(w, got_out, got_lse, ref_out, ref_lse, 1e3)
+
+
+def _assert_within_mean_abs_v(w, got_out, got_lse, ref_out, ref_lse, min_peak):
+    """Values of both signs far above the outputs: an output element is a weighted mean whose
+    terms are up to ~10^6 times larger than the mean itself, so the error of any fp32
+    accumulation scales with the mean of |V| under the same weights, not with |out|. That
+    mean is the oracle's decode of the same cache with the NoPE sign bits cleared (q_nope =
+    0: the weights depend on the RoPE part only)."""
+    layout = w.cfg.layout
     nope = workloads._NOPE[layout]
     kv_abs = w.kv_cache.copy()
     rb, ps = workloads._ROW_BYTES[layout], w.cfg.page_size
@@ -119,10 +124,54 @@ def test_decode_all_codes_wide_scales(layout, mode):
     rows[:, :, :nope] &= 0x7F
     kv_abs[:, :ps * rb] = rows.reshape(kv_abs.shape[0], ps * rb)
     mag, _ = oracle_decode(w, kv=kv_abs)
-    assert np.abs(ref_out).max() > 1e3, "the wide scales must reach the outputs"
+    assert np.abs(ref_out).max() > min_peak, "the wide scales must reach the outputs"
     assert np.all(np.isfinite(got_out))
     err = np.abs(got_out - ref_out)
     bound = 1e-2 * np.maximum(1.0, np.abs(mag))
     worst = np.unravel_index(np.argmax(err / bound), err.shape)
     assert np.all(err <= bound), f"layout {layout}: err {err[worst]:.3g} against mean |V| {mag[worst]:.3g}"
     assert np.abs(got_lse - ref_lse).max() <= 1e-3
+
+
+def _row_max_raises(w, threshold_log2):
+    """Per query row, how often a 64-row tile's largest score (log2 units) exceeds the running
+    maximum by more than threshold_log2, the running maximum starting at the first tile's
+    and moving only then (scores from the oracle's dequantised rows)."""
+    c = w.cfg
+    counts = []
+    for b in range(c.batch):
+        L = int(w.seqlens[b])
+        K = oracle.kv_gather(w.kv_cache, c.layout, c.page_size, w.block_table[b], L)
+        q = (w.q[b].reshape(-1, w.q.shape[-1]).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        s = (q @ K.T) * c.sm_scale * np.log2(np.e)
+        for r in range(s.shape[0]):
+            m, n = s[r, :64].max(), 0
+            for t0 in range(64, L, 64):
+                mt = s[r, t0:t0 + 64].max()
+                if mt > m + threshold_log2:
+                    m, n = mt, n + 1
+            counts.append(n)
+    return np.array(counts)
+
+
+@pytest.mark.parametrize("layout", [1, 2])
+def test_decode_wide_scales_with_rescales(layout):
+    # values up to 448 * 2^31 (scale bytes 150..158) while the RoPE scores grow along the
+    # sequence (RoPE part of row j scaled by 1 + j/8, q's RoPE part 2, q_nope 0): every query
+    # row's running maximum rises past the single-SM kernel's lazy-rescale threshold (2^64),
+    # so O^T is rescaled in TMEM while holding values near 2^64 x 2^10 rows x 2^40, inside
+    # fp32 by the kernel's range rule (rows x max|V| < 2^64)
+    from test_gpu_parity import _scale_rope_with_position
+    cfg = workloads.dsv4(batch=2, seqlens=(640, 1000), len_dist="fixed", page_size=64, layout=layout, heads=64,
+                         sink=False)
+    w = workloads.generate(cfg)
+    w = _rewrite_fp8(w, np.random.default_rng(300 + layout), 150, 158, with_nan=False)
+    _scale_rope_with_position(w, workloads._ROW_BYTES[layout], workloads._NOPE[layout], 8)
+    q = _scaled_q(w, 0.0, 1.0)
+    q[..., -64:] = np.uint16(0x4000)  # bf16 2.0
+    w = dataclasses.replace(w, q=q)
+    assert _row_max_raises(w, 64.0).min() >= 1
+    d = DeviceWorkload(w)
+    got_out, got_lse = d.run(write=False)
+    ref_out, ref_lse = oracle_decode(w, kv=w.kv_cache)
+    _assert_within_mean_abs_v(w, got_out, got_lse, ref_out, ref_lse, 1e6)
